@@ -1,0 +1,349 @@
+#!/usr/bin/env python3
+"""Throughput of the keyed BLAKE3 digest of one buffer resident in GPU memory.
+
+One step = one pass of the whole path over the 12 GiB + 777 byte workload
+(uniform bytes, data seed 6, key seed 7): the leaf kernel (chunk compression fused
+with the CTA subtree) followed by the reduction of the CTA roots to the ROOT digest.
+The input (12.9 GB) is far larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `value` is GB/s hashed (10^9 bytes of input per second) with
+the input already in HBM; `e2e` is the same metric through the public C-ABI call
+with the input copied from pinned host memory every step and the digest read back;
+`roofline` relates the leaf kernel (the dominant one) to the integer-issue peak of
+the GPU; `cpu_baseline` times the CPU oracle on a bounded prefix of the workload.
+`--impl reference` times the CPU oracle alone as the reference arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+
+from blake3_merkle_tree_gb300 import workloads  # noqa: E402
+
+METRIC = "GB/s hashed (keyed BLAKE3, 1 GB300)"
+WORKLOAD = "12GiB+777"
+# Integer work of one compression under the plain instruction count: 7 rounds x 8 G
+# x 12 operations (6 adds with the two 3-input adds fused, 4 XORs, 4 rotates ->
+# 2 IADD3 + 2 IADD + 4 XOR + 4 rotates) + 8 XORs for the output CV.
+OPS_PER_COMPRESSION = 7 * 8 * 12 + 8
+# The page's count ("7 rounds x 8 G x 6 operations = 336 per 64-byte block").
+PAGE_OPS_PER_COMPRESSION = 336
+INT32_LANES_PER_SM = 128  # integer instructions issued per SM per clock (4 schedulers x 32 lanes)
+
+
+def _peaks():
+    p = os.path.join(HERE, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="b3g_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.gpu and self.gpu.lower() not in parts[0].lower():
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 0.5 * max(x[2] for x in rows)] or rows
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in loaded for n, v in zip(names, r[3][1:]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(loaded), "reasons": reasons}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _oracle_sample(host_bytes: torch.Tensor, key: bytes, target_s: float):
+    """Time the CPU oracle on doubling prefixes until one run takes >= target_s."""
+    import oracle
+
+    n = min(64 << 20, host_bytes.numel())
+    while True:
+        t0 = time.perf_counter()
+        oracle.keyed_hash(host_bytes[:n], key)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or n >= host_bytes.numel():
+            return n, dt
+        n = min(host_bytes.numel(), n * max(2, int(target_s / max(dt, 1e-3) * 0.9)))
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, timed on the host cores, on bounded prefixes."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+
+    w = workloads.WORKLOADS[WORKLOAD]
+    key = w.key()
+    # size the per-step sample so that warm-up + timed steps take about a minute
+    probe = workloads.uniform_bytes(w.data_seed, 16 << 20)
+    t0 = time.perf_counter()
+    oracle.keyed_hash(probe, key)
+    speed = probe.numel() / (time.perf_counter() - t0)
+    budget_s = float(os.environ.get("B3G_REF_BUDGET_S", "60"))
+    sample = int(speed * budget_s / (args.steps + args.warmup))
+    sample = max(1 << 20, min(w.nbytes, sample - sample % 1024))
+    host = workloads.uniform_bytes(w.data_seed, sample)
+    for _ in range(args.warmup):
+        oracle.keyed_hash(host, key)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.keyed_hash(host, key)
+    dt = time.perf_counter() - t0
+    value = args.steps * sample / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} keyed BLAKE3, uniform bytes seed 6, key seed 7",
+                   "bytes": w.nbytes, "sample_bytes_per_step": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {sample} bytes of the workload, hashed as a whole input, per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    from blake3_merkle_tree_gb300 import binding, build
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    lib = binding.library()
+
+    w = workloads.WORKLOADS[WORKLOAD]
+    key = w.key()
+    n = w.nbytes
+    dev = w.data(device="cuda")
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    leaves_log2 = lib.blake3_default_leaves_log2()
+    tiles = lib.blake3_tile_count(n, leaves_log2)
+    roots = torch.empty((tiles, 32), dtype=torch.uint8, device="cuda")
+    red_ws = torch.empty(max(16, lib.blake3_reduce_workspace_size(tiles, -1)), dtype=torch.uint8, device="cuda")
+    out = torch.empty(32, dtype=torch.uint8, device="cuda")
+    kp = key
+
+    def step(ev_a=None, ev_b=None):
+        if ev_a is not None:
+            ev_a.record(stream)
+        st = lib.blake3_keyed_tile_roots(dev.data_ptr(), n, 0, kp, leaves_log2, 1, roots.data_ptr(), sp)
+        if st:
+            raise binding.B3GError(st, "blake3_keyed_tile_roots")
+        if ev_b is not None:
+            ev_b.record(stream)
+        if tiles > 1:
+            st = lib.blake3_keyed_reduce_cvs(roots.data_ptr(), tiles, kp, 1, -1, out.data_ptr(), red_ws.data_ptr(),
+                                             red_ws.numel(), sp)
+            if st:
+                raise binding.B3GError(st, "blake3_keyed_reduce_cvs")
+
+    # reduction launches per step: ceil-divide by 1024 until one CV is left
+    launches = 1
+    c = tiles
+    while c > 1:
+        c = -(-c // 1024)
+        launches += 1
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    digest_bench = bytes((roots[0] if tiles == 1 else out).cpu().numpy())
+    digest_api = bytes(binding.blake3_keyed_hash(dev, key).cpu().numpy())
+    if digest_bench != digest_api:
+        raise RuntimeError("bench step and blake3_keyed_hash disagree")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    gpu_id = str(getattr(props, "uuid", "") or "")
+    with ClockSampler(gpu_id) as clk:
+        for i in range(args.steps):
+            step(starts[i], mids[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = starts[0].elapsed_time(end)
+    leaf_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * n * args.steps / (total_ms / 1e3) / 1e9
+
+    # roofline of the leaf kernel (integer issue bound)
+    nchunks = max(1, -(-n // 1024))
+    nfull = n // 1024
+    tail = n % 1024
+    leaf_compressions = nfull * 16 + ((tail + 63) // 64 if tail else 0) + (nchunks - tiles)
+    ops = leaf_compressions * OPS_PER_COMPRESSION
+    page_ops = leaf_compressions * PAGE_OPS_PER_COMPRESSION
+    leaf_s = statistics.mean(leaf_ms) / 1e3
+    peaks, peak_kind = _peaks()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    clocks = clk.summary()
+    peak_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    int_peak = sms * INT32_LANES_PER_SM * peak_mhz * 1e6  # ops/s
+    achieved = ops / leaf_s
+    roofline = {
+        "bound": "alu", "achieved": achieved / 1e9, "peak": int_peak / 1e9, "unit": "Gop/s",
+        "frac": achieved / int_peak, "traffic": None,
+        "ops_per_launch": ops, "ops_per_byte": ops / n, "leaf_ms": statistics.mean(leaf_ms),
+        "peak_basis": f"{sms} SMs x {INT32_LANES_PER_SM} int32 lanes x {peak_mhz:.0f} MHz (derived)",
+        "page_count": {"ops_per_byte": page_ops / n, "achieved": page_ops / leaf_s / 1e9,
+                       "frac": page_ops / leaf_s / int_peak},
+        "hbm": {"achieved": n / leaf_s / 1e9, "peak": float(peaks.get("hbm_gbs", 6800.0)), "unit": "GB/s",
+                "frac": n / leaf_s / 1e9 / float(peaks.get("hbm_gbs", 6800.0)), "peak_kind": peak_kind},
+        "roofline_gbs": min(float(peaks.get("hbm_gbs", 6800.0)), int_peak / (ops / n) / 1e9),
+    }
+    roofline["frac_of_min_roofline"] = (n / leaf_s / 1e9) / roofline["roofline_gbs"]
+
+    # end to end through the public call, host buffers, copies inside the timed region
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    host = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    host.copy_(dev)
+    host_out = torch.empty(32, dtype=torch.uint8, pin_memory=True)
+    torch.cuda.synchronize()
+    for _ in range(1):
+        dev.copy_(host, non_blocking=True)
+        binding.blake3_keyed_hash(dev, key, out=out)
+        host_out.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dev.copy_(host, non_blocking=True)
+        binding.blake3_keyed_hash(dev, key, out=out)
+        host_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if bytes(host_out.numpy()) != digest_api:
+        raise RuntimeError("end-to-end digest differs")
+    e2e = {"value": world * n / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": n,
+           "d2h_bytes_per_step": 32, "ms_per_step": e2e_ms, "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample, dt = _oracle_sample(host, key, args.cpu_seconds)
+        cpu = {"value": sample / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {sample} bytes of the workload hashed as one input by the single-threaded "
+                         f"C oracle ({dt:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} keyed BLAKE3, uniform bytes seed 6, key seed 7", "bytes": n,
+                   "chunks": nchunks, "leaves_per_cta": 1 << leaves_log2, "cta_roots": tiles,
+                   "l2": "input 12.9 GB > 126 MB L2; no flush needed", "parallelism": f"replicas{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches * args.steps, "clocks": clocks,
+        "digest": digest_api.hex(),
+    }
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -22,6 +22,8 @@ _BINDING_NAMES = (
     "blake3_keyed_reduce_cvs",
     "blake3_reduce_workspace_size",
     "blake3_device_status",
+    "blake3_selftest_bounded_wait",
+    "blake3_tile_count",
     "blake3_strerror",
     "B3GError",
     "library",

@@ -1,0 +1,216 @@
+"""ctypes binding of libb3g.so: the C ABI of include/blake3_gb300.h, same names.
+
+Argument marshalling only (torch tensors -> device pointers and byte counts, key
+bytes, the current CUDA stream); every step of the computation runs in the CUDA
+library.  There is no fallback: if the library is missing or a call fails, the
+call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libb3g.so")
+
+B3G_OK = 0
+B3G_DEVICE_STATUS_TIMEOUT = 1
+STATUS_NAMES = {0: "B3G_OK", 1: "B3G_ERR_NULL", 2: "B3G_ERR_ALIGN", 3: "B3G_ERR_WORKSPACE",
+                4: "B3G_ERR_CUDA", 5: "B3G_ERR_TIMEOUT", 6: "B3G_ERR_ARG"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class B3GError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {STATUS_NAMES.get(status, status)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+def library() -> ctypes.CDLL:
+    """Load libb3g.so (it must have been built, e.g. by __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libb3g.so not built at {LIB_PATH}; run blake3_merkle_tree_gb300.build")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, u64, i32, sz = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int, ctypes.c_size_t
+        sigs = {
+            "blake3_strerror": (ctypes.c_char_p, [i32]),
+            "blake3_last_cuda_error": (ctypes.c_char_p, []),
+            "blake3_default_leaves_log2": (i32, []),
+            "blake3_keyed_hash": (i32, [vp, u64, vp, vp, vp]),
+            "blake3_workspace_size": (sz, [u64]),
+            "blake3_keyed_hash_ws": (i32, [vp, u64, vp, vp, vp, sz, vp]),
+            "blake3_keyed_chunk_cvs": (i32, [vp, u64, u64, vp, vp, vp]),
+            "blake3_keyed_subtree_root": (i32, [vp, u64, u64, vp, i32, vp, vp]),
+            "blake3_tile_count": (u64, [u64, i32]),
+            "blake3_keyed_tile_roots": (i32, [vp, u64, u64, vp, i32, i32, vp, vp]),
+            "blake3_reduce_workspace_size": (sz, [u64, i32]),
+            "blake3_keyed_reduce_cvs": (i32, [vp, u64, vp, i32, i32, vp, vp, sz, vp]),
+            "blake3_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32)]),
+            "blake3_selftest_bounded_wait": (i32, [ctypes.c_uint32, ctypes.POINTER(ctypes.c_int)]),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != B3G_OK:
+        detail = library().blake3_last_cuda_error().decode() if status == 4 else ""
+        raise B3GError(status, where, detail)
+
+
+def _dev_ptr(t: torch.Tensor | None, what: str):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t.data_ptr() if t.numel() else None
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def _key(key) -> bytes:
+    key = bytes(key)
+    if len(key) != 32:
+        raise ValueError("key must be 32 bytes")
+    return key
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _out32(out: torch.Tensor | None, like: torch.Tensor | None) -> torch.Tensor:
+    if out is None:
+        dev = like.device if like is not None and like.is_cuda else torch.device("cuda")
+        out = torch.empty(32, dtype=torch.uint8, device=dev)
+    if _nbytes(out) < 32:
+        raise ValueError("output needs 32 bytes")
+    return out
+
+
+def blake3_strerror(status: int) -> str:
+    return library().blake3_strerror(status).decode()
+
+
+def blake3_workspace_size(nbytes: int) -> int:
+    return int(library().blake3_workspace_size(nbytes))
+
+
+def blake3_reduce_workspace_size(count: int, group_log2: int = -1) -> int:
+    return int(library().blake3_reduce_workspace_size(count, group_log2))
+
+
+def blake3_keyed_hash(data: torch.Tensor, key, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Digest of the bytes of the contiguous CUDA tensor `data` (32-byte uint8 tensor)."""
+    out = _out32(out, data)
+    st = library().blake3_keyed_hash(_dev_ptr(data, "data"), _nbytes(data), _key(key), _dev_ptr(out, "out"),
+                                     _stream(stream))
+    _check(st, "blake3_keyed_hash")
+    return out
+
+
+def blake3_keyed_hash_ws(data: torch.Tensor, key, workspace: torch.Tensor | None,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    out = _out32(out, data)
+    ws_ptr = _dev_ptr(workspace, "workspace") if workspace is not None else None
+    ws_bytes = _nbytes(workspace) if workspace is not None else 0
+    st = library().blake3_keyed_hash_ws(_dev_ptr(data, "data"), _nbytes(data), _key(key), _dev_ptr(out, "out"),
+                                        ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "blake3_keyed_hash_ws")
+    return out
+
+
+def blake3_keyed_chunk_cvs(data: torch.Tensor, key, chunk_offset: int = 0, out: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """All chunk CVs as a (n_chunks, 32) uint8 CUDA tensor."""
+    n = max(1, -(-_nbytes(data) // 1024))
+    if out is None:
+        out = torch.empty((n, 32), dtype=torch.uint8, device=data.device)
+    if _nbytes(out) < 32 * n:
+        raise ValueError("chunk CV output too small")
+    st = library().blake3_keyed_chunk_cvs(_dev_ptr(data, "data"), _nbytes(data), chunk_offset, _key(key),
+                                          _dev_ptr(out, "out"), _stream(stream))
+    _check(st, "blake3_keyed_chunk_cvs")
+    return out
+
+
+def blake3_keyed_subtree_root(data: torch.Tensor, key, chunk_offset: int = 0, is_root: bool = False,
+                              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    out = _out32(out, data)
+    st = library().blake3_keyed_subtree_root(_dev_ptr(data, "data"), _nbytes(data), chunk_offset, _key(key),
+                                             int(is_root), _dev_ptr(out, "out"), _stream(stream))
+    _check(st, "blake3_keyed_subtree_root")
+    return out
+
+
+def blake3_tile_count(nbytes: int, leaves_log2: int = -1) -> int:
+    return int(library().blake3_tile_count(nbytes, leaves_log2))
+
+
+def blake3_keyed_tile_roots(data: torch.Tensor, key, chunk_offset: int = 0, leaves_log2: int = -1,
+                            is_root: bool = False, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """CTA subtree roots as a (tiles, 32) uint8 CUDA tensor."""
+    tiles = blake3_tile_count(_nbytes(data), leaves_log2)
+    if tiles == 0:
+        raise B3GError(6, "blake3_keyed_tile_roots", "leaves_log2 out of range")
+    if out is None:
+        out = torch.empty((tiles, 32), dtype=torch.uint8, device=data.device)
+    if _nbytes(out) < 32 * tiles:
+        raise ValueError("tile root output too small")
+    st = library().blake3_keyed_tile_roots(_dev_ptr(data, "data"), _nbytes(data), chunk_offset, _key(key),
+                                           leaves_log2, int(is_root), _dev_ptr(out, "out"), _stream(stream))
+    _check(st, "blake3_keyed_tile_roots")
+    return out
+
+
+def blake3_keyed_reduce_cvs(cvs: torch.Tensor, key, is_root: bool = False, group_log2: int = -1,
+                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """Reduce a (count, 32) uint8 CUDA tensor of subtree CVs to one CV."""
+    count = _nbytes(cvs) // 32
+    out = _out32(out, cvs)
+    if workspace is None:
+        need = blake3_reduce_workspace_size(count, group_log2) if count else 0
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=cvs.device)
+    st = library().blake3_keyed_reduce_cvs(_dev_ptr(cvs, "cvs"), count, _key(key), int(is_root), group_log2,
+                                           _dev_ptr(out, "out"), _dev_ptr(workspace, "workspace"),
+                                           _nbytes(workspace), _stream(stream))
+    _check(st, "blake3_keyed_reduce_cvs")
+    return out
+
+
+def blake3_device_status() -> int:
+    v = ctypes.c_uint32(0)
+    _check(library().blake3_device_status(ctypes.byref(v)), "blake3_device_status")
+    return int(v.value)
+
+
+def blake3_selftest_bounded_wait(limit_us: int) -> bool:
+    flag = ctypes.c_int(-1)
+    _check(library().blake3_selftest_bounded_wait(limit_us, ctypes.byref(flag)), "blake3_selftest_bounded_wait")
+    return flag.value == 1

@@ -1,0 +1,326 @@
+// b3g_api.cu -- the C ABI of libb3g.so (declared in include/blake3_gb300.h).
+//
+// Host-side planning only: argument checks, the chunk/tile arithmetic, workspace
+// layout and the kernel launches.  All hashing runs on the GPU.
+//
+// Call structure (source page "BLAKE3 GPU 400x faster hashing", sections
+// "我们的实现", "Kernel 1", "Kernel 2 和 3"):
+//   1. leaf kernel: chunk CVs and the fused CTA subtree -> one CV per tile of 2^t
+//      chunks (or the digest itself when the input fits one tile);
+//   2. reduction kernel, relaunched on its own output until one CV remains; the
+//      launch with a single group sets ROOT.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "b3g_internal.h"
+
+namespace b3g {
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+// Device status word: bit B3G_DEVICE_STATUS_TIMEOUT is set by a kernel whose
+// bounded wait gave up.  One per device (a module-scope variable lives in every
+// device's copy of the module).
+__device__ uint32_t g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+b3g_status status_word(uint32_t **out) {
+    static std::mutex mu;
+    static uint32_t *cache[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return B3G_ERR_ARG;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_status);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        cache[dev] = static_cast<uint32_t *>(p);
+    }
+    *out = cache[dev];
+    return B3G_OK;
+}
+
+uint64_t n_chunks_of(uint64_t len) { return len == 0 ? 1 : (len + kChunkBytes - 1) / kChunkBytes; }
+
+uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+
+void key_words(const uint8_t key[32], uint32_t out[8]) {
+    for (int i = 0; i < 8; ++i)
+        out[i] = static_cast<uint32_t>(key[4 * i]) | (static_cast<uint32_t>(key[4 * i + 1]) << 8) |
+                 (static_cast<uint32_t>(key[4 * i + 2]) << 16) | (static_cast<uint32_t>(key[4 * i + 3]) << 24);
+}
+
+bool valid_leaves_log2(int t) { return t >= kMinLeavesLog2 && t <= kMaxLeavesLog2; }
+
+// Outputs and CV inputs are moved with 16-byte vector accesses.
+bool misaligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+size_t round16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+// Bytes for the intermediate levels of a reduction of `count` CVs with groups of
+// 2^g: every level except the last (which writes the final output) needs a buffer.
+size_t reduce_ws(uint64_t count, int g) {
+    size_t total = 0;
+    uint64_t c = count;
+    const uint64_t group = 1ull << g;
+    while (c > group) {
+        c = ceil_div(c, group);
+        total += round16(c * 32);
+    }
+    return total;
+}
+
+// Reduce `count` CVs at d_cvs into d_out32 (see blake3_keyed_reduce_cvs).
+b3g_status reduce_levels(const uint8_t *d_cvs, uint64_t count, const uint32_t key[8], bool is_root, int g,
+                         uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
+    if (count == 1) {
+        cudaError_t e = cudaMemcpyAsync(d_out32, d_cvs, 32, cudaMemcpyDeviceToDevice, stream);
+        return e == cudaSuccess ? B3G_OK : cuda_fail(e, "cudaMemcpyAsync");
+    }
+    const uint64_t group = 1ull << g;
+    const uint8_t *cur = d_cvs;
+    uint64_t c = count;
+    uint8_t *next_buf = ws;
+    while (true) {
+        ReduceArgs ra;
+        ra.in = cur;
+        ra.count = c;
+        const uint64_t groups = ceil_div(c, group);
+        ra.out = groups == 1 ? d_out32 : next_buf;
+        std::memcpy(ra.key, key, sizeof ra.key);
+        ra.root = is_root ? 1u : 0u;
+        ra.group = static_cast<uint32_t>(group);
+        b3g_status st = launch_reduce(ra, stream);
+        if (st != B3G_OK) return st;
+        if (groups == 1) return B3G_OK;
+        cur = next_buf;
+        next_buf += round16(groups * 32);
+        c = groups;
+    }
+}
+
+LeafArgs leaf_args(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32], int t,
+                   bool root, uint8_t *out, uint32_t *status) {
+    LeafArgs a;
+    a.in = static_cast<const uint8_t *>(d_in);
+    a.len = len;
+    a.n_chunks = n_chunks_of(len);
+    a.n_full = len / kChunkBytes;
+    a.counter_base = chunk_offset;
+    a.n_tiles = ceil_div(a.n_chunks, 1ull << t);
+    a.out = out;
+    a.status = status;
+    a.wait_limit_ns = kWaitLimitNs;
+    key_words(key, a.key);
+    a.root = root ? 1u : 0u;
+    a.tail_bytes = static_cast<uint32_t>(len % kChunkBytes);
+    return a;
+}
+
+// The whole path: leaf kernel, then the reduction levels.  `ws` must hold
+// blake3_workspace_size(len) bytes when more than one tile exists.
+b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32], bool root,
+                      uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
+    uint32_t *status = nullptr;
+    b3g_status st = status_word(&status);
+    if (st != B3G_OK) return st;
+    const int t = kDefaultLeavesLog2;
+    LeafArgs a = leaf_args(d_in, len, chunk_offset, key, t, root, nullptr, status);
+    if (a.n_tiles == 1) {
+        a.out = d_out32;
+        return launch_leaf(a, t, false, stream);
+    }
+    a.out = ws;
+    st = launch_leaf(a, t, false, stream);
+    if (st != B3G_OK) return st;
+    return reduce_levels(ws, a.n_tiles, a.key, root, kDefaultGroupLog2, d_out32,
+                         ws + round16(a.n_tiles * 32), stream);
+}
+
+size_t hash_workspace(uint64_t len) {
+    const uint64_t tiles = ceil_div(n_chunks_of(len), 1ull << kDefaultLeavesLog2);
+    if (tiles == 1) return 0;
+    return round16(tiles * 32) + reduce_ws(tiles, kDefaultGroupLog2);
+}
+
+// Runs hash_range with a stream-ordered temporary workspace.
+b3g_status hash_range_alloc(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
+                            bool root, uint8_t *d_out32, cudaStream_t stream) {
+    const size_t need = hash_workspace(len);
+    void *ws = nullptr;
+    if (need) {
+        cudaError_t e = cudaMallocAsync(&ws, need, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
+    }
+    b3g_status st = hash_range(d_in, len, chunk_offset, key, root, d_out32, static_cast<uint8_t *>(ws), stream);
+    if (ws) {
+        cudaError_t e = cudaFreeAsync(ws, stream);
+        if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
+    }
+    return st;
+}
+
+}  // namespace
+
+b3g_status cuda_fail(cudaError_t err, const char *what) {
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s (%d)", what, cudaGetErrorString(err),
+                  static_cast<int>(err));
+    return B3G_ERR_CUDA;
+}
+
+}  // namespace b3g
+
+using namespace b3g;
+
+extern "C" {
+
+const char *blake3_strerror(b3g_status s) {
+    switch (s) {
+        case B3G_OK: return "success";
+        case B3G_ERR_NULL: return "a required pointer is NULL";
+        case B3G_ERR_ALIGN: return "misaligned argument (chunk_offset, workspace or a 16-byte aligned pointer)";
+        case B3G_ERR_WORKSPACE: return "workspace too small";
+        case B3G_ERR_CUDA: return "CUDA runtime error";
+        case B3G_ERR_TIMEOUT: return "a device-side bounded wait gave up";
+        case B3G_ERR_ARG: return "argument out of range";
+    }
+    return "unknown status";
+}
+
+const char *blake3_last_cuda_error(void) { return g_last_cuda_error; }
+
+int blake3_default_leaves_log2(void) { return kDefaultLeavesLog2; }
+
+size_t blake3_workspace_size(uint64_t len) { return hash_workspace(len); }
+
+b3g_status blake3_keyed_hash(const void *d_in, uint64_t len, const uint8_t key[32], uint8_t *d_out32,
+                             b3g_stream_t stream) {
+    if (!key || !d_out32 || (!d_in && len > 0)) return B3G_ERR_NULL;
+    if (misaligned16(d_out32)) return B3G_ERR_ALIGN;
+    return hash_range_alloc(d_in, len, 0, key, true, d_out32, reinterpret_cast<cudaStream_t>(stream));
+}
+
+b3g_status blake3_keyed_hash_ws(const void *d_in, uint64_t len, const uint8_t key[32], uint8_t *d_out32,
+                                void *d_ws, size_t ws_bytes, b3g_stream_t stream) {
+    if (!key || !d_out32 || (!d_in && len > 0)) return B3G_ERR_NULL;
+    if (misaligned16(d_out32)) return B3G_ERR_ALIGN;
+    const size_t need = hash_workspace(len);
+    if (need) {
+        if (!d_ws || ws_bytes < need) return B3G_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(d_ws) & 15u) return B3G_ERR_ALIGN;
+    }
+    return hash_range(d_in, len, 0, key, true, d_out32, static_cast<uint8_t *>(d_ws),
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+b3g_status blake3_keyed_chunk_cvs(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
+                                  uint8_t *d_cvs, b3g_stream_t stream) {
+    if (!key || !d_cvs || (!d_in && len > 0)) return B3G_ERR_NULL;
+    if (misaligned16(d_cvs)) return B3G_ERR_ALIGN;
+    uint32_t *status = nullptr;
+    b3g_status st = status_word(&status);
+    if (st != B3G_OK) return st;
+    LeafArgs a = leaf_args(d_in, len, chunk_offset, key, kDefaultLeavesLog2, false, d_cvs, status);
+    return launch_leaf(a, kDefaultLeavesLog2, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+b3g_status blake3_keyed_subtree_root(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
+                                     int is_root, uint8_t *d_out32, b3g_stream_t stream) {
+    if (!key || !d_out32 || (!d_in && len > 0)) return B3G_ERR_NULL;
+    if (misaligned16(d_out32)) return B3G_ERR_ALIGN;
+    const uint64_t n = n_chunks_of(len);
+    uint64_t p = 1;
+    while (p < n) p <<= 1;
+    if (chunk_offset % p != 0) return B3G_ERR_ALIGN;
+    return hash_range_alloc(d_in, len, chunk_offset, key, is_root != 0, d_out32,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+uint64_t blake3_tile_count(uint64_t len, int leaves_log2) {
+    if (leaves_log2 == -1) leaves_log2 = kDefaultLeavesLog2;
+    if (!valid_leaves_log2(leaves_log2)) return 0;
+    return ceil_div(n_chunks_of(len), 1ull << leaves_log2);
+}
+
+b3g_status blake3_keyed_tile_roots(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
+                                   int leaves_log2, int is_root, uint8_t *d_roots, b3g_stream_t stream) {
+    if (!key || !d_roots || (!d_in && len > 0)) return B3G_ERR_NULL;
+    if (misaligned16(d_roots)) return B3G_ERR_ALIGN;
+    if (leaves_log2 == -1) leaves_log2 = kDefaultLeavesLog2;
+    if (!valid_leaves_log2(leaves_log2)) return B3G_ERR_ARG;
+    uint32_t *status = nullptr;
+    b3g_status st = status_word(&status);
+    if (st != B3G_OK) return st;
+    LeafArgs a = leaf_args(d_in, len, chunk_offset, key, leaves_log2, is_root != 0, d_roots, status);
+    return launch_leaf(a, leaves_log2, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t blake3_reduce_workspace_size(uint64_t count, int group_log2) {
+    if (group_log2 == -1) group_log2 = kDefaultGroupLog2;
+    if (group_log2 < 1 || group_log2 > kMaxGroupLog2 || count == 0) return 0;
+    return reduce_ws(count, group_log2);
+}
+
+b3g_status blake3_keyed_reduce_cvs(const uint8_t *d_cvs, uint64_t count, const uint8_t key[32], int is_root,
+                                   int group_log2, uint8_t *d_out32, void *d_ws, size_t ws_bytes,
+                                   b3g_stream_t stream) {
+    if (!key || !d_cvs || !d_out32) return B3G_ERR_NULL;
+    if (misaligned16(d_cvs) || misaligned16(d_out32)) return B3G_ERR_ALIGN;
+    if (group_log2 == -1) group_log2 = kDefaultGroupLog2;
+    if (count == 0 || group_log2 < 1 || group_log2 > kMaxGroupLog2) return B3G_ERR_ARG;
+    if (count == 1 && is_root) return B3G_ERR_ARG;
+    const size_t need = reduce_ws(count, group_log2);
+    if (need) {
+        if (!d_ws || ws_bytes < need) return B3G_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(d_ws) & 15u) return B3G_ERR_ALIGN;
+    }
+    uint32_t kw[8];
+    key_words(key, kw);
+    return reduce_levels(d_cvs, count, kw, is_root != 0, group_log2, d_out32, static_cast<uint8_t *>(d_ws),
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+b3g_status blake3_device_status(uint32_t *status_out) {
+    if (!status_out) return B3G_ERR_NULL;
+    uint32_t *status = nullptr;
+    b3g_status st = status_word(&status);
+    if (st != B3G_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    uint32_t v = 0;
+    e = cudaMemcpy(&v, status, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+    e = cudaMemset(status, 0, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    *status_out = v;
+    return B3G_OK;
+}
+
+b3g_status blake3_selftest_bounded_wait(uint32_t limit_us, int *timed_out_out) {
+    if (!timed_out_out) return B3G_ERR_NULL;
+    if (limit_us < 1 || limit_us > 10000000u) return B3G_ERR_ARG;
+    int *d_flag = nullptr;
+    cudaError_t e = cudaMalloc(&d_flag, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    b3g_status st = launch_wait_probe(static_cast<uint64_t>(limit_us) * 1000ull, d_flag, nullptr);
+    int h = -1;
+    if (st == B3G_OK) {
+        e = cudaMemcpy(&h, d_flag, sizeof h, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) st = cuda_fail(e, "cudaMemcpy(flag)");
+    }
+    cudaFree(d_flag);
+    if (st == B3G_OK) *timed_out_out = h;
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,346 @@
+// b3g_device.cuh -- device building blocks for the keyed BLAKE3 kernels (sm_103a).
+//
+// Source page: "BLAKE3 GPU 400x faster hashing" (qfminer.top).
+//   section "压缩函数": one thread compresses one chunk entirely in registers, the
+//     round function fully unrolled; 16 chained compressions per chunk, CHUNK_START
+//     on the first block and CHUNK_END on the last; the key is the initial CV.
+//   section "Merkle Tree 归约": parent = compress(key, left || right, counter 0,
+//     length 64, KEYED_HASH | PARENT); halving levels with a barrier between them;
+//     non-power-of-two leaf counts fold the binary decomposition right to left.
+//   section "未来工作": exchange CVs between threads with warp primitives instead
+//     of shared memory during the reduction.
+// Round constants follow the BLAKE3 specification (O'Connor et al., 2020).
+#pragma once
+
+#include <cstdint>
+
+namespace b3g {
+
+// ---------------------------------------------------------------------------------
+// Constants of the BLAKE3 specification.
+// ---------------------------------------------------------------------------------
+constexpr uint32_t kChunkLen = 1024;
+constexpr uint32_t kBlockLen = 64;
+
+constexpr uint32_t kIv0 = 0x6A09E667u, kIv1 = 0xBB67AE85u, kIv2 = 0x3C6EF372u, kIv3 = 0xA54FF53Au;
+
+constexpr uint32_t kChunkStart = 1u, kChunkEnd = 2u, kParent = 4u, kRoot = 8u, kKeyedHash = 16u;
+
+// Message word that G-slot i reads in round r: the message is permuted between
+// rounds by P (word i of the next round is word P[i] of this one), so round r
+// reads original word P^r(i).  Evaluated at compile time; with the rounds fully
+// unrolled the permutation is pure register renaming.
+__host__ __device__ constexpr int msg_index(int round, int slot) {
+    constexpr int P[16] = {2, 6, 3, 10, 7, 0, 4, 13, 1, 11, 12, 5, 9, 14, 15, 8};
+    int i = slot;
+    for (int r = 0; r < round; ++r) i = P[i];
+    return i;
+}
+
+// ---------------------------------------------------------------------------------
+// Rotations: byte permutes for 16 and 8, funnel shifts for 12 and 7.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t rotr16(uint32_t x) { return __byte_perm(x, 0, 0x1032); }
+__device__ __forceinline__ uint32_t rotr8(uint32_t x) { return __byte_perm(x, 0, 0x0321); }
+__device__ __forceinline__ uint32_t rotr12(uint32_t x) { return __funnelshift_r(x, x, 12); }
+__device__ __forceinline__ uint32_t rotr7(uint32_t x) { return __funnelshift_r(x, x, 7); }
+
+__device__ __forceinline__ void g(uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d, uint32_t x,
+                                  uint32_t y) {
+    a = a + b + x;
+    d = rotr16(d ^ a);
+    c = c + d;
+    b = rotr12(b ^ c);
+    a = a + b + y;
+    d = rotr8(d ^ a);
+    c = c + d;
+    b = rotr7(b ^ c);
+}
+
+template <int R>
+__device__ __forceinline__ void round_fn(uint32_t v[16], const uint32_t m[16]) {
+    // columns
+    g(v[0], v[4], v[8], v[12], m[msg_index(R, 0)], m[msg_index(R, 1)]);
+    g(v[1], v[5], v[9], v[13], m[msg_index(R, 2)], m[msg_index(R, 3)]);
+    g(v[2], v[6], v[10], v[14], m[msg_index(R, 4)], m[msg_index(R, 5)]);
+    g(v[3], v[7], v[11], v[15], m[msg_index(R, 6)], m[msg_index(R, 7)]);
+    // diagonals
+    g(v[0], v[5], v[10], v[15], m[msg_index(R, 8)], m[msg_index(R, 9)]);
+    g(v[1], v[6], v[11], v[12], m[msg_index(R, 10)], m[msg_index(R, 11)]);
+    g(v[2], v[7], v[8], v[13], m[msg_index(R, 12)], m[msg_index(R, 13)]);
+    g(v[3], v[4], v[9], v[14], m[msg_index(R, 14)], m[msg_index(R, 15)]);
+}
+
+// One compression; cv (8 words) is replaced by the first 8 output words.
+__device__ __forceinline__ void compress(uint32_t cv[8], const uint32_t m[16], uint32_t counter_lo,
+                                         uint32_t counter_hi, uint32_t block_len, uint32_t flags) {
+    uint32_t v[16] = {cv[0], cv[1], cv[2],      cv[3],      cv[4],     cv[5], cv[6], cv[7],
+                      kIv0,  kIv1,  kIv2,       kIv3,       counter_lo, counter_hi, block_len, flags};
+    round_fn<0>(v, m);
+    round_fn<1>(v, m);
+    round_fn<2>(v, m);
+    round_fn<3>(v, m);
+    round_fn<4>(v, m);
+    round_fn<5>(v, m);
+    round_fn<6>(v, m);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cv[i] = v[i] ^ v[i + 8];
+}
+
+// Parent node: key as CV, left || right as the message.
+__device__ __forceinline__ void parent(const uint32_t key[8], const uint32_t l[8], const uint32_t r[8],
+                                       bool root, uint32_t out[8]) {
+    uint32_t m[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        m[i] = l[i];
+        m[i + 8] = r[i];
+    }
+    uint32_t cv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cv[i] = key[i];
+    compress(cv, m, 0u, 0u, kBlockLen, kKeyedHash | kParent | (root ? kRoot : 0u));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = cv[i];
+}
+
+// ---------------------------------------------------------------------------------
+// Shared-memory, barrier and bulk-tensor-copy primitives (inline PTX).
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait until the barrier phase with the given parity has completed, or give up
+// after limit_ns nanoseconds.  Returns false if it gave up.  Every wait in the
+// hashing kernels goes through here, so no kernel can spin forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// 2-D tiled bulk tensor copy global -> shared, completion signalled on `bar`
+// through the transaction count.  x is the innermost (word) coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t x, int32_t y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier over `nthreads` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t res;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(res)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+        : "memory");
+    return res != 0;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------------
+// Loads of one 64-byte block straight from global memory, for the partial last
+// chunk and for inputs that cannot use the bulk tensor copy.  Bytes at or beyond
+// `len` read as zero, and no byte outside [base, base + len) is touched.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t load_byte(const uint8_t *base, uint64_t len, uint64_t off) {
+    return off < len ? static_cast<uint32_t>(__ldg(base + off)) : 0u;
+}
+
+__device__ __forceinline__ void load_block_global(const uint8_t *base, uint64_t len, uint64_t off,
+                                                  uint32_t m[16]) {
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(base) + off;
+    if (off + kBlockLen <= len && (addr & 15u) == 0) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(base + off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 w = __ldg(p + q);
+            m[4 * q + 0] = w.x;
+            m[4 * q + 1] = w.y;
+            m[4 * q + 2] = w.z;
+            m[4 * q + 3] = w.w;
+        }
+        return;
+    }
+    const uintptr_t lo = addr & ~static_cast<uintptr_t>(3);
+    const uintptr_t hi = (addr + kBlockLen + 3) & ~static_cast<uintptr_t>(3);
+    const uintptr_t buf_lo = reinterpret_cast<uintptr_t>(base);
+    const uintptr_t buf_hi = buf_lo + len;
+    if (lo >= buf_lo && hi <= buf_hi) {
+        // every aligned word covering the block lies inside the buffer
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(lo);
+        const uint32_t sh = static_cast<uint32_t>(addr & 3u) * 8u;
+        uint32_t prev = __ldg(w);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            uint32_t next = (sh == 0 && i == 15) ? 0u : __ldg(w + i + 1);
+            m[i] = sh == 0 ? prev : __funnelshift_r(prev, next, sh);
+            prev = next;
+        }
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint64_t o = off + 4u * i;
+        m[i] = load_byte(base, len, o) | (load_byte(base, len, o + 1) << 8) |
+               (load_byte(base, len, o + 2) << 16) | (load_byte(base, len, o + 3) << 24);
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// CV nodes in shared memory.  Node j occupies 16-byte units 2j and 2j+1; unit k is
+// stored at k with its low three bits XORed by bits 3..5 (a 128-byte swizzle), so
+// that both "thread j writes node j" and "thread t reads nodes 2t, 2t+1" touch 32
+// distinct banks per quarter-warp.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t node_unit_addr(uint32_t base, uint32_t unit) {
+    const uint32_t phys = unit ^ ((unit >> 3) & 7u);
+    return base + phys * 16u;
+}
+
+__device__ __forceinline__ void store_node(uint32_t base, uint32_t j, const uint32_t cv[8]) {
+    sts128(node_unit_addr(base, 2 * j), make_uint4(cv[0], cv[1], cv[2], cv[3]));
+    sts128(node_unit_addr(base, 2 * j + 1), make_uint4(cv[4], cv[5], cv[6], cv[7]));
+}
+
+__device__ __forceinline__ void load_node(uint32_t base, uint32_t j, uint32_t cv[8]) {
+    uint4 a = lds128(node_unit_addr(base, 2 * j));
+    uint4 b = lds128(node_unit_addr(base, 2 * j + 1));
+    cv[0] = a.x; cv[1] = a.y; cv[2] = a.z; cv[3] = a.w;
+    cv[4] = b.x; cv[5] = b.y; cv[6] = b.z; cv[7] = b.w;
+}
+
+// ---------------------------------------------------------------------------------
+// Tree reduction of `cnt` consecutive nodes into one (page section
+// "Merkle Tree 归约").  Each level pairs nodes (2j, 2j+1); when a level has an odd
+// count its last node moves up unchanged.  Level-order pairing with that
+// carry-up builds exactly the tree of the binary decomposition folded right to
+// left: after level L the array holds the perfect 2^L subtrees of the aligned
+// prefix followed, if the count is not a multiple of 2^L, by the right fold of the
+// remainder; pairing the last perfect subtree with that fold is the next step of
+// the right-to-left fold.
+//
+// Levels with more than 32 nodes run in shared memory with the active threads
+// packed into whole warps; once 32 nodes or fewer are left, warp 0 holds one node
+// per lane and finishes with shuffles, without shared memory or barriers.  ROOT
+// goes on the final compression when `root` is set.
+// ---------------------------------------------------------------------------------
+
+// Warp-level part: lane j holds node j (j < cnt); on return lane 0 holds the root.
+__device__ __forceinline__ void warp_tree(uint32_t x[8], uint32_t cnt, const uint32_t key[8], bool root) {
+    const uint32_t lane = threadIdx.x & 31u;
+    while (cnt > 1) {
+        const uint32_t half = cnt >> 1;
+        uint32_t l[8], r[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            l[w] = __shfl_sync(0xffffffffu, x[w], (2 * lane) & 31u);
+            r[w] = __shfl_sync(0xffffffffu, x[w], (2 * lane + 1) & 31u);
+        }
+        if (lane < half) {
+            parent(key, l, r, root && cnt == 2, x);
+        } else if (lane == half && (cnt & 1u)) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) x[w] = l[w];  // node cnt-1 moves up
+        }
+        cnt = (cnt + 1) >> 1;
+    }
+}
+
+// Block-level part, over the `nthreads` threads that share named barrier `bar_id`.
+// On entry node j (j < cnt) is in `nodes` and a barrier has made the stores
+// visible.  On return lane 0 of warp 0 (thread 0) holds the root in out[8]; the
+// node buffer may be reused after the call.
+__device__ __forceinline__ void block_tree(uint32_t nodes, uint32_t cnt, uint32_t tid, uint32_t nthreads,
+                                           uint32_t bar_id, const uint32_t key[8], bool root,
+                                           uint32_t out[8]) {
+    while (cnt > 32) {
+        const uint32_t half = cnt >> 1;
+        uint32_t res[8];
+        bool have = false;
+        if (tid < half) {
+            uint32_t l[8], r[8];
+            load_node(nodes, 2 * tid, l);
+            load_node(nodes, 2 * tid + 1, r);
+            parent(key, l, r, false, res);
+            have = true;
+        } else if (tid == half && (cnt & 1u)) {
+            load_node(nodes, cnt - 1, res);
+            have = true;
+        }
+        named_bar_sync(bar_id, nthreads);
+        if (have) store_node(nodes, tid, res);
+        named_bar_sync(bar_id, nthreads);
+        cnt = (cnt + 1) >> 1;
+    }
+    if (tid < 32) {
+        if (tid < cnt) load_node(nodes, tid, out);
+    }
+    named_bar_sync(bar_id, nthreads);  // the node buffer is free again
+    if (tid < 32) warp_tree(out, cnt, key, root);
+}
+
+}  // namespace b3g

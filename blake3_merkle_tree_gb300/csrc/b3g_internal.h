@@ -1,0 +1,65 @@
+// b3g_internal.h -- launch-level interface between the C ABI (b3g_api.cu) and the
+// kernel translation units (b3g_leaf.cu, b3g_reduce.cu).  Not installed.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/blake3_gb300.h"
+
+namespace b3g {
+
+constexpr uint64_t kChunkBytes = 1024;
+constexpr int kMinLeavesLog2 = 5;
+constexpr int kMaxLeavesLog2 = 8;
+constexpr int kDefaultLeavesLog2 = 8;
+constexpr int kMaxGroupLog2 = 10;
+constexpr int kDefaultGroupLog2 = 10;
+// Default limit of every device-side wait: far above any real wait (microseconds),
+// far below a hang.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Arguments of the leaf kernels (page section "Kernel 1": every CTA compresses a
+// group of 2^t chunks and reduces them to one subtree CV).
+struct LeafArgs {
+    const uint8_t *in;      // device bytes
+    uint64_t len;           // bytes
+    uint64_t n_chunks;      // max(1, ceil(len / 1024))
+    uint64_t n_full;        // len / 1024: chunks that are complete
+    uint64_t counter_base;  // global index of the first chunk
+    uint64_t n_tiles;       // ceil(n_chunks / 2^t)
+    uint8_t *out;           // tile CVs (32 B each) or chunk CVs (32 B each)
+    uint32_t *status;       // device status word
+    uint64_t wait_limit_ns;
+    uint32_t key[8];
+    uint32_t root;        // ROOT on the final compression if the whole tree is one tile
+    uint32_t tail_bytes;  // bytes of the partial last chunk; 0 if none
+};
+
+// Arguments of the CV reduction kernel (page section "Kernel 2 和 3").
+struct ReduceArgs {
+    const uint8_t *in;  // count CVs
+    uint64_t count;
+    uint8_t *out;       // ceil(count / group) CVs
+    uint32_t key[8];
+    uint32_t root;      // ROOT on the final compression when one group remains
+    uint32_t group;     // CVs per CTA, a power of two in 2..1024
+};
+
+// Launches the leaf kernel: per tile CVs (chunk_cvs == false) or per chunk CVs.
+// Chooses the bulk-tensor-copy path when `in` is 16-byte aligned and holds at
+// least one full chunk, the plain-load path otherwise.
+b3g_status launch_leaf(const LeafArgs &args, int leaves_log2, bool chunk_cvs, cudaStream_t stream);
+
+// One level of CV reduction.
+b3g_status launch_reduce(const ReduceArgs &args, cudaStream_t stream);
+
+// One-thread bounded-wait probe; writes 1 to *d_flag if the wait gave up.
+b3g_status launch_wait_probe(uint64_t limit_ns, int *d_flag, cudaStream_t stream);
+
+// Records a CUDA error for blake3_last_cuda_error() and returns B3G_ERR_CUDA.
+b3g_status cuda_fail(cudaError_t err, const char *what);
+
+}  // namespace b3g

@@ -1,0 +1,432 @@
+// b3g_leaf.cu -- leaf kernels: chunk compression fused with the CTA subtree.
+//
+// Source page: "BLAKE3 GPU 400x faster hashing" (qfminer.top).
+//   section "Kernel 1": each CTA takes 2^t consecutive chunks, one consumer thread
+//     per chunk, and reduces their CVs to one subtree CV without a round trip
+//     through global memory; a producer loads the data with the tensor memory
+//     accelerator (TMA).
+//   section "TMA 加载": global memory is viewed as a (chunks, 256) matrix of 32-bit
+//     words; one load brings a (2^t, words-per-load) tile, 128 bytes of every chunk.
+//   section "消费者循环": consumers wait for a stage, read it with 128-bit shared
+//     loads, compress, and release the stage to the producer.
+//   section "共享内存布局与 Swizzle": stage buffers are swizzled so that the
+//     consumers' row reads avoid bank conflicts.
+//   section "不完整块的处理": the last CTA may hold fewer chunks, and the last chunk
+//     may be partial; the partial chunk is zero padded.
+//
+// GB300 design (differences from the page's Hopper design):
+//   - Persistent CTAs: the grid is sized to the resident capacity and each CTA walks
+//     tiles blockIdx.x, blockIdx.x + gridDim.x, ...; the stage ring keeps running
+//     across tiles, so the producer loads the next tile during the subtree phase.
+//   - One producer warp (one elected lane) instead of 128 producer threads; the
+//     consumers release a stage per warp (one arrive per warp on the "empty"
+//     barrier) instead of a consumer-wide barrier.
+//   - The box height is at most 256 rows (the TMA limit), so one tensor map and one
+//     pipeline cover every tile size up to 256 chunks; no dual pipeline is needed.
+//   - The partial last chunk is not padded inside the stage: rows past the last full
+//     chunk are outside the tensor map, which the TMA fills with zeros, and the one
+//     thread that owns the partial chunk reads its bytes from global memory with
+//     bounds checks (zero beyond the end of the input).
+//   - Every barrier wait is bounded in time; a wait that gives up sets the device
+//     status word and the CTA leaves after draining its copies in flight.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "b3g_device.cuh"
+#include "b3g_internal.h"
+
+namespace b3g {
+
+constexpr uint32_t kBarTree = 1;  // named barrier id of the consumer threads
+
+// ---------------------------------------------------------------------------------
+// Bulk-tensor-copy (TMA) pipeline kernel.
+//   C          consumers = chunks per tile (2^t), a multiple of 32, at most 256
+//   S          stages in the shared-memory ring
+//   LOAD       bytes of every chunk brought by one load (128 or 64)
+//   CHUNK_CVS  write every chunk CV instead of reducing the tile
+// ---------------------------------------------------------------------------------
+template <int C, int S, int LOAD, bool CHUNK_CVS>
+struct TmaCfg {
+    static_assert(C % 32 == 0 && C >= 32 && C <= 256, "consumer count");
+    static_assert(LOAD == 128 || LOAD == 64, "load width");
+    static constexpr int kLoadsPerTile = 1024 / LOAD;
+    static constexpr int kBlocksPerLoad = LOAD / 64;
+    static constexpr uint32_t kStageBytes = C * LOAD;
+    static constexpr int kConsumerWarps = C / 32;
+    static constexpr int kThreads = C + 32;
+    static constexpr uint32_t kNodeBytes = C * 32;
+    // stages (1024-aligned for the swizzle), nodes, then 2*S barriers
+    static constexpr size_t kSmemBytes = 1024 + size_t(S) * kStageBytes + kNodeBytes + 16 * S;
+    // The single node buffer is reused tile after tile.  A consumer warp can only
+    // run ahead of the slowest one by S loads, so with S < kLoadsPerTile no warp
+    // can reach the next tile's node stores while warp 0 still reads the previous
+    // tile's nodes (block_tree also ends with a barrier after that read).
+    static_assert(S >= 2 && S < kLoadsPerTile, "stage count");
+};
+
+template <int C, int S, int LOAD, bool CHUNK_CVS>
+__global__ void __launch_bounds__(C + 32)
+    leaf_tma_kernel(const __grid_constant__ CUtensorMap tmap, const LeafArgs a) {
+    using Cfg = TmaCfg<C, S, LOAD, CHUNK_CVS>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t stage0 = (raw + 1023u) & ~1023u;
+    const uint32_t nodes = stage0 + S * Cfg::kStageBytes;
+    const uint32_t full0 = nodes + Cfg::kNodeBytes;  // S barriers, 8 bytes each
+    const uint32_t empty0 = full0 + 8 * S;
+
+    const uint32_t tid = threadIdx.x;
+    const uint32_t warp = tid >> 5;
+    const uint32_t lane = tid & 31u;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, Cfg::kConsumerWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == Cfg::kConsumerWarps) {
+        // ------------------------------- producer -------------------------------
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap) : "memory");
+            uint32_t it = 0;
+            bool ok = true;
+            for (uint64_t tile = blockIdx.x; ok && tile < a.n_tiles; tile += gridDim.x) {
+                for (int ld = 0; ld < Cfg::kLoadsPerTile; ++ld, ++it) {
+                    const uint32_t s = it % S;
+                    const uint32_t k = it / S;
+                    if (k > 0 && !mbar_wait_bounded(empty0 + 8 * s, (k - 1) & 1u, a.wait_limit_ns)) {
+                        atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full0 + 8 * s, Cfg::kStageBytes);
+                    tma_load_2d(stage0 + s * Cfg::kStageBytes, &tmap, ld * (LOAD / 4),
+                                static_cast<int32_t>(tile * C), full0 + 8 * s);
+                }
+            }
+            // Drain: wait (bounded) for the last loads issued, so that no copy into
+            // this CTA's shared memory is still in flight when it exits.  On the
+            // normal path the consumers have already waited for them.
+            const uint32_t inflight = it < S ? it : S;
+            for (uint32_t j = 0; j < inflight; ++j) {
+                const uint32_t u = it - 1 - j;
+                mbar_wait_bounded(full0 + 8 * (u % S), (u / S) & 1u, a.wait_limit_ns);
+            }
+        }
+        return;
+    }
+
+    // --------------------------------- consumers ---------------------------------
+    uint32_t key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) key[i] = a.key[i];
+    const uint32_t r = tid;
+    // 16-byte unit u of this thread's row sits at u ^ swz (TMA 128B / 64B swizzle)
+    const uint32_t swz = LOAD == 128 ? (r & 7u) : ((r >> 1) & 3u);
+    const uint32_t row_off = r * LOAD;
+    uint32_t it = 0;
+    bool aborted = false;
+
+    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+        const uint64_t chunk = tile * C + r;
+        const bool valid = chunk < a.n_chunks;
+        const bool is_tail = a.tail_bytes != 0 && chunk == a.n_full;
+        const uint32_t nblocks = is_tail ? (a.tail_bytes + 63u) / 64u : 16u;
+        const uint32_t last_len = is_tail ? a.tail_bytes - 64u * (nblocks - 1u) : 64u;
+        const uint64_t ctr = a.counter_base + chunk;
+        const uint32_t ctr_lo = static_cast<uint32_t>(ctr);
+        const uint32_t ctr_hi = static_cast<uint32_t>(ctr >> 32);
+        const uint32_t end_flags = kChunkEnd | ((a.root && a.n_chunks == 1) ? kRoot : 0u);
+
+        uint32_t cv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cv[i] = key[i];
+
+#pragma unroll 1
+        for (int ld = 0; ld < Cfg::kLoadsPerTile; ++ld, ++it) {
+            const uint32_t s = it % S;
+            const uint32_t k = it / S;
+            if (aborted) continue;
+            if (!mbar_wait_bounded(full0 + 8 * s, k & 1u, a.wait_limit_ns)) {
+                atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
+                aborted = true;
+                continue;
+            }
+            const uint32_t rowp = stage0 + s * Cfg::kStageBytes + row_off;
+#pragma unroll
+            for (int j = 0; j < Cfg::kBlocksPerLoad; ++j) {
+                const uint32_t b = ld * Cfg::kBlocksPerLoad + j;
+                uint32_t m[16];
+                if (!is_tail) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t u = static_cast<uint32_t>(4 * j + q);
+                        const uint4 w = lds128(rowp + ((u ^ swz) << 4));
+                        m[4 * q + 0] = w.x;
+                        m[4 * q + 1] = w.y;
+                        m[4 * q + 2] = w.z;
+                        m[4 * q + 3] = w.w;
+                    }
+                } else {
+                    load_block_global(a.in, a.len, chunk * kChunkBytes + 64ull * b, m);
+                }
+                const bool last = b + 1 == nblocks;
+                const uint32_t flags = kKeyedHash | (b == 0 ? kChunkStart : 0u) | (last ? end_flags : 0u);
+                if (b < nblocks) compress(cv, m, ctr_lo, ctr_hi, last ? last_len : 64u, flags);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        }
+
+        if constexpr (CHUNK_CVS) {
+            if (aborted) break;
+            if (valid) {
+                uint4 *o = reinterpret_cast<uint4 *>(a.out + chunk * 32);
+                o[0] = make_uint4(cv[0], cv[1], cv[2], cv[3]);
+                o[1] = make_uint4(cv[4], cv[5], cv[6], cv[7]);
+            }
+        } else {
+            if (valid) store_node(nodes, r, cv);
+            // barrier before the tree; also makes the abort decision uniform
+            if (named_bar_or(kBarTree, C, aborted)) break;
+            const uint64_t rem = a.n_chunks - tile * C;
+            const uint32_t cnt = rem < C ? static_cast<uint32_t>(rem) : static_cast<uint32_t>(C);
+            uint32_t root_cv[8];
+            block_tree(nodes, cnt, r, C, kBarTree, key, a.root && a.n_tiles == 1, root_cv);
+            if (r == 0) {
+                uint4 *o = reinterpret_cast<uint4 *>(a.out + tile * 32);
+                o[0] = make_uint4(root_cv[0], root_cv[1], root_cv[2], root_cv[3]);
+                o[1] = make_uint4(root_cv[4], root_cv[5], root_cv[6], root_cv[7]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// Plain-load kernel: any alignment, any length (including 0 and inputs without a
+// full chunk).  Same tiles and subtree as the TMA kernel; each thread reads its
+// chunk's blocks from global memory with bounds checks.
+// ---------------------------------------------------------------------------------
+template <int C, bool CHUNK_CVS>
+__global__ void __launch_bounds__(C) leaf_direct_kernel(const LeafArgs a) {
+    __shared__ __align__(128) uint8_t node_mem[C * 32];
+    const uint32_t nodes = smem_u32(node_mem);
+    uint32_t key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) key[i] = a.key[i];
+    const uint32_t r = threadIdx.x;
+
+    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+        const uint64_t chunk = tile * C + r;
+        const bool valid = chunk < a.n_chunks;
+        const uint64_t start = chunk * kChunkBytes;
+        const uint64_t rest = (valid && start < a.len) ? a.len - start : 0;
+        const uint32_t bytes = rest < kChunkBytes ? static_cast<uint32_t>(rest) : 1024u;
+        const uint32_t nblocks = bytes == 0 ? 1u : (bytes + 63u) / 64u;
+        const uint32_t last_len = bytes - 64u * (nblocks - 1u);
+        const uint64_t ctr = a.counter_base + chunk;
+        const uint32_t end_flags = kChunkEnd | ((a.root && a.n_chunks == 1) ? kRoot : 0u);
+        uint32_t cv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cv[i] = key[i];
+        if (valid) {
+#pragma unroll 1
+            for (uint32_t b = 0; b < nblocks; ++b) {
+                uint32_t m[16];
+                load_block_global(a.in, a.len, start + 64ull * b, m);
+                const bool last = b + 1 == nblocks;
+                const uint32_t flags = kKeyedHash | (b == 0 ? kChunkStart : 0u) | (last ? end_flags : 0u);
+                compress(cv, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32),
+                         last ? last_len : 64u, flags);
+            }
+        }
+        if constexpr (CHUNK_CVS) {
+            if (valid) {
+                uint4 *o = reinterpret_cast<uint4 *>(a.out + chunk * 32);
+                o[0] = make_uint4(cv[0], cv[1], cv[2], cv[3]);
+                o[1] = make_uint4(cv[4], cv[5], cv[6], cv[7]);
+            }
+        } else {
+            if (valid) store_node(nodes, r, cv);
+            named_bar_sync(kBarTree, C);
+            const uint64_t rem = a.n_chunks - tile * C;
+            const uint32_t cnt = rem < C ? static_cast<uint32_t>(rem) : static_cast<uint32_t>(C);
+            uint32_t root_cv[8];
+            block_tree(nodes, cnt, r, C, kBarTree, key, a.root && a.n_tiles == 1, root_cv);
+            if (r == 0) {
+                uint4 *o = reinterpret_cast<uint4 *>(a.out + tile * 32);
+                o[0] = make_uint4(root_cv[0], root_cv[1], root_cv[2], root_cv[3]);
+                o[1] = make_uint4(root_cv[4], root_cv[5], root_cv[6], root_cv[7]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------------
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Stage count and load width per tile size (chosen by measurement on GB300).
+template <int C>
+struct Tuning;
+template <>
+struct Tuning<256> {
+    static constexpr int S = 3, LOAD = 128;
+};
+template <>
+struct Tuning<128> {
+    static constexpr int S = 4, LOAD = 128;
+};
+template <>
+struct Tuning<64> {
+    static constexpr int S = 4, LOAD = 128;
+};
+template <>
+struct Tuning<32> {
+    static constexpr int S = 4, LOAD = 128;
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+struct DeviceInfo {
+    int sm_count = 0;
+};
+
+b3g_status device_info(int dev, DeviceInfo &out) {
+    static std::mutex mu;
+    static DeviceInfo cache[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return B3G_ERR_ARG;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].sm_count == 0) {
+        int sms = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        cache[dev].sm_count = sms;
+    }
+    out = cache[dev];
+    return B3G_OK;
+}
+
+// Per-device, per-kernel launch set-up: the shared-memory opt-in and the number of
+// resident CTAs per SM (the persistent grid is that times the SM count).
+b3g_status kernel_blocks_per_sm(const void *kernel, int threads, size_t smem, int dev, int &blocks) {
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({kernel, dev});
+    if (it != cache.end()) {
+        blocks = it->second;
+        return B3G_OK;
+    }
+    cudaError_t e;
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    }
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (n < 1) return cuda_fail(cudaErrorInvalidConfiguration, "occupancy is zero");
+    cache[{kernel, dev}] = n;
+    blocks = n;
+    return B3G_OK;
+}
+
+uint64_t grid_for(uint64_t n_tiles, int blocks_per_sm, int sms) {
+    const uint64_t cap = static_cast<uint64_t>(blocks_per_sm) * static_cast<uint64_t>(sms);
+    return n_tiles < cap ? n_tiles : cap;
+}
+
+template <int C, bool CV>
+b3g_status launch_tma(const LeafArgs &a, cudaStream_t stream, int dev, const DeviceInfo &info) {
+    using T = Tuning<C>;
+    using Cfg = TmaCfg<C, T::S, T::LOAD, CV>;
+    auto kernel = leaf_tma_kernel<C, T::S, T::LOAD, CV>;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+    if (!encode) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled unavailable");
+    CUtensorMap tmap;
+    cuuint64_t gdim[2] = {256, static_cast<cuuint64_t>(a.n_full)};
+    cuuint64_t gstride[1] = {1024};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(T::LOAD / 4), static_cast<cuuint32_t>(C)};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t *>(a.in), gdim, gstride,
+                         box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         T::LOAD == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+    int bps = 0;
+    b3g_status st = kernel_blocks_per_sm(reinterpret_cast<const void *>(kernel), Cfg::kThreads, Cfg::kSmemBytes, dev, bps);
+    if (st != B3G_OK) return st;
+    const uint64_t grid = grid_for(a.n_tiles, bps, info.sm_count);
+    kernel<<<static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tmap, a);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "leaf_tma_kernel launch");
+}
+
+template <int C, bool CV>
+b3g_status launch_direct(const LeafArgs &a, cudaStream_t stream, int dev, const DeviceInfo &info) {
+    auto kernel = leaf_direct_kernel<C, CV>;
+    int bps = 0;
+    b3g_status st = kernel_blocks_per_sm(reinterpret_cast<const void *>(kernel), C, 0, dev, bps);
+    if (st != B3G_OK) return st;
+    const uint64_t grid = grid_for(a.n_tiles, bps, info.sm_count);
+    kernel<<<static_cast<unsigned>(grid), C, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "leaf_direct_kernel launch");
+}
+
+template <int C>
+b3g_status launch_c(const LeafArgs &a, bool chunk_cvs, bool tma, cudaStream_t stream, int dev,
+                    const DeviceInfo &info) {
+    if (tma) return chunk_cvs ? launch_tma<C, true>(a, stream, dev, info) : launch_tma<C, false>(a, stream, dev, info);
+    return chunk_cvs ? launch_direct<C, true>(a, stream, dev, info) : launch_direct<C, false>(a, stream, dev, info);
+}
+
+}  // namespace
+
+b3g_status launch_leaf(const LeafArgs &a, int leaves_log2, bool chunk_cvs, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DeviceInfo info;
+    b3g_status st = device_info(dev, info);
+    if (st != B3G_OK) return st;
+    // The tensor map needs a 16-byte aligned base, at least one full chunk, and
+    // row coordinates that fit in int32.
+    const bool tma = a.n_full >= 1 && (reinterpret_cast<uintptr_t>(a.in) & 15u) == 0 &&
+                     a.n_full + 256 < (1ull << 31);
+    switch (leaves_log2) {
+        case 5: return launch_c<32>(a, chunk_cvs, tma, stream, dev, info);
+        case 6: return launch_c<64>(a, chunk_cvs, tma, stream, dev, info);
+        case 7: return launch_c<128>(a, chunk_cvs, tma, stream, dev, info);
+        case 8: return launch_c<256>(a, chunk_cvs, tma, stream, dev, info);
+        default: return B3G_ERR_ARG;
+    }
+}
+
+}  // namespace b3g

@@ -1,0 +1,187 @@
+/*
+ * blake3_gb300.h -- C ABI of libb3g.so: the keyed BLAKE3 digest of one buffer that
+ * already sits in GPU memory, computed by hand-written sm_103a (GB300) kernels.
+ *
+ * What is computed (source page: "BLAKE3 GPU 400x faster hashing", qfminer.top):
+ *   - section "BLAKE3": the input is cut into 1024-byte chunks and each chunk into
+ *     64-byte blocks; each block is compressed (7 rounds) with the running chaining
+ *     value (CV), a per-chunk counter, the block length and flags; the key is the
+ *     starting CV (keyed mode, the only mode the page uses); the chunk CVs are then
+ *     paired into parent nodes until one CV is left, with a full left subtree of a
+ *     power-of-two chunk count that is at least as large as its right sibling.
+ *   - section "压缩函数": CHUNK_START on a chunk's first block, CHUNK_END on its last.
+ *   - section "Merkle Tree 归约": parents use counter 0, block length 64 and flags
+ *     KEYED_HASH|PARENT; non-power-of-two counts fold their binary decomposition
+ *     from right to left.
+ *   - section "Kernel 2 和 3": ROOT is set on the final compression only.
+ *   - section "不完整块的处理": the last chunk (and block) may be partial; it is
+ *     zero padded and its block length is its true byte count.
+ *   The round constants (IV, G rotations, message permutation, flag bit values)
+ *   are those of the published BLAKE3 specification (O'Connor et al., 2020).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named d_* are DEVICE pointers on the current CUDA device; `key` is a
+ *     HOST pointer to 32 bytes, copied into the launch parameters before the call
+ *     returns (it may be freed right after).  Byte strings (key, CVs, digest) are
+ *     32 bytes, little-endian words, exactly as BLAKE3 defines them.
+ *   - The caller owns every buffer.  Nothing is retained across calls except a
+ *     per-device cache of launch settings and the device status word.
+ *   - All calls that take a stream are asynchronous on it: no host synchronisation
+ *     and no device-to-host copy.  Errors found on the host (arguments, launch)
+ *     are returned; errors found on the device (a bounded wait that gave up) are
+ *     recorded in the device status word, read by blake3_device_status().
+ *   - len == 0 is valid (the empty input has one empty chunk); d_in may then be NULL.
+ *   - d_in may have any alignment.  A 16-byte aligned d_in with at least one full
+ *     chunk takes the bulk-tensor-copy (TMA) path; other inputs take a path with
+ *     plain bounds-checked loads.  Both give identical results.
+ *   - Device pointers that receive CVs or a digest (d_out32, d_cvs, d_roots), and
+ *     the CVs given to blake3_keyed_reduce_cvs, must be 16-byte aligned (they are
+ *     moved with 16-byte vector accesses); otherwise the call returns B3G_ERR_ALIGN.
+ *   - A call never aborts the process; it returns a b3g_status.
+ */
+#ifndef BLAKE3_GB300_H
+#define BLAKE3_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *b3g_stream_t;
+
+typedef enum {
+    B3G_OK = 0,
+    B3G_ERR_NULL = 1,      /* a required pointer is NULL */
+    B3G_ERR_ALIGN = 2,     /* chunk_offset not a multiple of the subtree's size, or a
+                              pointer lacks the 16-byte alignment it needs */
+    B3G_ERR_WORKSPACE = 3, /* the workspace given is smaller than required */
+    B3G_ERR_CUDA = 4,      /* a CUDA runtime call failed (see blake3_last_cuda_error) */
+    B3G_ERR_TIMEOUT = 5,   /* a device-side bounded wait gave up (device status word) */
+    B3G_ERR_ARG = 6,       /* an argument is out of range */
+} b3g_status;
+
+/* Bit set in the device status word when a kernel's bounded wait gave up. */
+#define B3G_DEVICE_STATUS_TIMEOUT 1u
+
+/* Static text for a status code; never NULL. */
+const char *blake3_strerror(b3g_status status);
+
+/* Text of the last CUDA error seen by this thread inside the library ("" if none). */
+const char *blake3_last_cuda_error(void);
+
+/* Chunks per CTA subtree used when leaves_log2 is -1 (a power of two: 2^8 = 256). */
+int blake3_default_leaves_log2(void);
+
+/*
+ * blake3_keyed_hash -- the digest of d_in[0..len) under `key`, written to d_out32.
+ * Page sections "BLAKE3" (chunking, tree rules), "Kernel 1" (leaf kernel with the
+ * fused subtree), "Kernel 2 和 3" (reduction of the subtree roots, ROOT last).
+ * Temporary device memory (32 bytes per 256 chunks) comes from the stream-ordered
+ * allocator (cudaMallocAsync/cudaFreeAsync on `stream`).
+ * Errors: B3G_ERR_NULL (key or d_out32 NULL, or d_in NULL with len > 0),
+ * B3G_ERR_CUDA.
+ */
+b3g_status blake3_keyed_hash(const void *d_in, uint64_t len, const uint8_t key[32],
+                             uint8_t *d_out32, b3g_stream_t stream);
+
+/* Bytes of device workspace blake3_keyed_hash_ws needs for a len-byte input
+ * (0 when the input fits one CTA subtree). */
+size_t blake3_workspace_size(uint64_t len);
+
+/*
+ * blake3_keyed_hash_ws -- as blake3_keyed_hash, with caller-provided device
+ * workspace d_ws of ws_bytes bytes (at least blake3_workspace_size(len), 16-byte
+ * aligned).  Performs no allocation.  Concurrent calls must not share d_ws.
+ * Errors: as blake3_keyed_hash, plus B3G_ERR_WORKSPACE (too small or NULL when
+ * needed) and B3G_ERR_ALIGN (d_ws not 16-byte aligned).
+ */
+b3g_status blake3_keyed_hash_ws(const void *d_in, uint64_t len, const uint8_t key[32],
+                                uint8_t *d_out32, void *d_ws, size_t ws_bytes,
+                                b3g_stream_t stream);
+
+/*
+ * blake3_keyed_chunk_cvs -- the CV of every chunk of d_in[0..len), none with ROOT,
+ * chunk i using counter chunk_offset + i (page section "压缩函数": one thread per
+ * chunk, 16 chained block compressions).  d_cvs receives max(1, ceil(len/1024))
+ * CVs of 32 bytes, in chunk order.
+ * Errors: B3G_ERR_NULL, B3G_ERR_CUDA.
+ */
+b3g_status blake3_keyed_chunk_cvs(const void *d_in, uint64_t len, uint64_t chunk_offset,
+                                  const uint8_t key[32], uint8_t *d_cvs, b3g_stream_t stream);
+
+/*
+ * blake3_keyed_subtree_root -- the CV of the subtree whose leaves are the chunks of
+ * d_in[0..len), the first chunk having global index chunk_offset.  With is_root != 0
+ * the final compression carries ROOT (then, with chunk_offset 0, this is the digest).
+ * The chunk range must be a subtree of the whole input's tree: chunk_offset must be
+ * a multiple of the smallest power of two >= the chunk count, and a partial last
+ * chunk or a non-power-of-two count is only valid for the input's last subtree (the
+ * caller's responsibility; it cannot be checked here).  Temporary memory as in
+ * blake3_keyed_hash.
+ * Errors: B3G_ERR_NULL, B3G_ERR_ALIGN (chunk_offset misaligned), B3G_ERR_CUDA.
+ */
+b3g_status blake3_keyed_subtree_root(const void *d_in, uint64_t len, uint64_t chunk_offset,
+                                     const uint8_t key[32], int is_root, uint8_t *d_out32,
+                                     b3g_stream_t stream);
+
+/* Number of CTA subtree roots blake3_keyed_tile_roots writes: ceil(chunks / 2^leaves_log2).
+ * Returns 0 for a leaves_log2 outside 5..8 (or -1 for the default). */
+uint64_t blake3_tile_count(uint64_t len, int leaves_log2);
+
+/*
+ * blake3_keyed_tile_roots -- the leaf kernel alone (page section "Kernel 1"): every
+ * aligned group of 2^leaves_log2 chunks (leaves_log2 in 5..8, or -1 for the default)
+ * is compressed and reduced inside one CTA to its subtree CV; the last group may be
+ * smaller and is folded right to left.  d_roots receives blake3_tile_count() CVs.
+ * chunk_offset as in blake3_keyed_subtree_root.  If there is a single group and
+ * is_root != 0, its CV is the finished digest (ROOT set on the final compression);
+ * with several groups is_root is ignored.
+ * Errors: B3G_ERR_NULL, B3G_ERR_ARG (leaves_log2), B3G_ERR_CUDA.
+ */
+b3g_status blake3_keyed_tile_roots(const void *d_in, uint64_t len, uint64_t chunk_offset,
+                                   const uint8_t key[32], int leaves_log2, int is_root,
+                                   uint8_t *d_roots, b3g_stream_t stream);
+
+/* Device workspace bytes blake3_keyed_reduce_cvs needs for `count` CVs and groups of
+ * 2^group_log2 (group_log2 in 1..10, or -1 for the default 10). */
+size_t blake3_reduce_workspace_size(uint64_t count, int group_log2);
+
+/*
+ * blake3_keyed_reduce_cvs -- reduce `count` (>= 1) consecutive subtree CVs d_cvs
+ * (the left-to-right leaves of one tree, each an aligned power-of-two subtree except
+ * possibly the last) to one CV in d_out32 (page section "Kernel 2 和 3"): each CTA
+ * reduces an aligned group of 2^group_log2 CVs, and launches repeat until one CV is
+ * left; with is_root != 0 the final compression carries ROOT.  count == 1 copies the
+ * CV (is_root must then be 0: ROOT cannot be added to a finished CV).
+ * Errors: B3G_ERR_NULL, B3G_ERR_ARG (count 0, group_log2, count 1 with is_root),
+ * B3G_ERR_WORKSPACE, B3G_ERR_ALIGN (d_ws not 16-byte aligned), B3G_ERR_CUDA.
+ */
+b3g_status blake3_keyed_reduce_cvs(const uint8_t *d_cvs, uint64_t count, const uint8_t key[32],
+                                   int is_root, int group_log2, uint8_t *d_out32, void *d_ws,
+                                   size_t ws_bytes, b3g_stream_t stream);
+
+/*
+ * blake3_device_status -- waits for the current device to go idle, stores the device
+ * status word (0, or B3G_DEVICE_STATUS_TIMEOUT) in *status_out and clears it.
+ * Errors: B3G_ERR_NULL, B3G_ERR_CUDA.
+ */
+b3g_status blake3_device_status(uint32_t *status_out);
+
+/*
+ * blake3_selftest_bounded_wait -- launches one thread that waits on a shared-memory
+ * barrier nobody arrives on, with a limit of limit_us microseconds (1..10^7), and
+ * stores 1 in *timed_out_out if the wait gave up (the expected outcome), else 0.
+ * This exercises the same bounded wait the hashing kernels use, so that the
+ * give-up path is tested without a hang.  Synchronous.  Does not touch the status
+ * word.  Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_CUDA.
+ */
+b3g_status blake3_selftest_bounded_wait(uint32_t limit_us, int *timed_out_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BLAKE3_GB300_H */

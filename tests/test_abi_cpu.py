@@ -1,0 +1,102 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and its
+host-side logic (sizes, argument checks that return before any CUDA call) works."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from blake3_merkle_tree_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every call below fails its checks first
+KEY = bytes(range(32))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("defined",):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from blake3_merkle_tree_gb300 import build
+
+    build.build()
+    return binding.library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert "blake3_keyed_hash" in names and len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror(lib):
+    for code in range(7):
+        assert lib.blake3_strerror(code)
+    assert lib.blake3_strerror(99) == b"unknown status"
+
+
+def test_sizes(lib):
+    assert lib.blake3_default_leaves_log2() == 8
+    assert lib.blake3_tile_count(0, -1) == 1
+    assert lib.blake3_tile_count(256 * 1024, -1) == 1
+    assert lib.blake3_tile_count(256 * 1024 + 1, -1) == 2
+    assert lib.blake3_tile_count(12 * (1 << 30) + 777, 8) == 49153
+    assert lib.blake3_tile_count(1 << 20, 5) == 32
+    assert lib.blake3_tile_count(1 << 20, 4) == 0
+    assert lib.blake3_workspace_size(256 * 1024) == 0  # one tile: no workspace
+    assert lib.blake3_workspace_size(1 << 20) == 4 * 32
+    # 4 GiB: 16384 tile CVs, then 16 group CVs
+    assert lib.blake3_workspace_size(1 << 32) == 16384 * 32 + 16 * 32
+    assert lib.blake3_reduce_workspace_size(1024, 10) == 0
+    assert lib.blake3_reduce_workspace_size(1025, 10) == 64
+    assert lib.blake3_reduce_workspace_size(5, 1) == 3 * 32 + 32 + 32
+
+
+def test_argument_errors_before_any_cuda_call(lib):
+    out = FAKE
+    assert lib.blake3_keyed_hash(FAKE, 10, None, out, None) == 1
+    assert lib.blake3_keyed_hash(None, 10, KEY, out, None) == 1
+    assert lib.blake3_keyed_hash(FAKE, 10, KEY, None, None) == 1
+    assert lib.blake3_keyed_hash_ws(FAKE, 1 << 30, KEY, out, None, 0, None) == 3
+    assert lib.blake3_keyed_hash_ws(FAKE, 1 << 30, KEY, out, FAKE, 16, None) == 3
+    assert lib.blake3_keyed_hash_ws(FAKE, 1 << 30, KEY, out, ctypes.c_void_p(0x10001), 1 << 20, None) == 2
+    assert lib.blake3_keyed_subtree_root(FAKE, 4 * 1024, 2, KEY, 0, out, None) == 2
+    assert lib.blake3_keyed_subtree_root(FAKE, 3 * 1024, 6, KEY, 0, out, None) == 2
+    assert lib.blake3_keyed_tile_roots(FAKE, 4096, 0, KEY, 9, 0, out, None) == 6
+    assert lib.blake3_keyed_tile_roots(FAKE, 4096, 0, KEY, 4, 0, out, None) == 6
+    assert lib.blake3_keyed_reduce_cvs(FAKE, 0, KEY, 0, -1, out, FAKE, 0, None) == 6
+    assert lib.blake3_keyed_reduce_cvs(FAKE, 1, KEY, 1, -1, out, FAKE, 0, None) == 6
+    assert lib.blake3_keyed_reduce_cvs(FAKE, 8, KEY, 1, 11, out, FAKE, 0, None) == 6
+    assert lib.blake3_keyed_reduce_cvs(FAKE, 5000, KEY, 1, 10, out, None, 0, None) == 3
+    assert lib.blake3_keyed_chunk_cvs(FAKE, 10, 0, KEY, None, None) == 1
+    assert lib.blake3_device_status(None) == 1
+    assert lib.blake3_selftest_bounded_wait(0, ctypes.byref(ctypes.c_int())) == 6
+    assert lib.blake3_selftest_bounded_wait(10, None) == 1
+
+
+def test_binding_refuses_host_tensors(lib):
+    import torch
+
+    with pytest.raises(ValueError):
+        binding.blake3_keyed_hash(torch.zeros(10, dtype=torch.uint8), KEY, out=torch.zeros(32, dtype=torch.uint8))
+
+
+def test_output_alignment_is_checked(lib):
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.blake3_keyed_hash(FAKE, 10, KEY, odd, None) == 2
+    assert lib.blake3_keyed_hash_ws(FAKE, 10, KEY, odd, None, 0, None) == 2
+    assert lib.blake3_keyed_chunk_cvs(FAKE, 10, 0, KEY, odd, None) == 2
+    assert lib.blake3_keyed_subtree_root(FAKE, 10, 0, KEY, 1, odd, None) == 2
+    assert lib.blake3_keyed_tile_roots(FAKE, 10, 0, KEY, -1, 1, odd, None) == 2
+    assert lib.blake3_keyed_reduce_cvs(odd, 4, KEY, 1, -1, FAKE, FAKE, 0, None) == 2

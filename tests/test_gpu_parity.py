@@ -1,0 +1,175 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle, bit-exact.
+
+Inputs are seeded and synthetic (blake3_merkle_tree_gb300.workloads).  Sizes span
+several CTA tiles and a ragged tail; the full-size workloads are in
+test_gpu_fullsize.py.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from blake3_merkle_tree_gb300 import binding, workloads
+
+pytestmark = pytest.mark.gpu
+
+KEY = workloads.key_bytes(1)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from blake3_merkle_tree_gb300 import build
+
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    binding.library()
+    yield
+    assert binding.blake3_device_status() == 0
+
+
+def _gpu_digest(host: torch.Tensor, key) -> bytes:
+    d = host.cuda()
+    out = binding.blake3_keyed_hash(d, key)
+    return bytes(out.cpu().numpy())
+
+
+def test_one_mib_config():
+    w = workloads.WORKLOADS["1MiB"]
+    data = w.data()
+    assert _gpu_digest(data, w.key()) == oracle.keyed_hash(data, w.key())
+
+
+@pytest.mark.parametrize("length", workloads.ragged_lengths())
+def test_ragged_sweep(length):
+    w = workloads.ragged_workload(length)
+    data = w.data()
+    assert _gpu_digest(data, w.key()) == oracle.keyed_hash(data, w.key()), length
+
+
+def test_empty_input_null_pointer():
+    out = torch.empty(32, dtype=torch.uint8, device="cuda")
+    st = binding.library().blake3_keyed_hash(None, 0, KEY, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    assert bytes(out.cpu().numpy()) == oracle.keyed_hash(b"", KEY)
+
+
+@pytest.mark.parametrize("length", [1, 63, 1024, 5000, 256 * 1024 + 3, 700 * 1024 + 100])
+@pytest.mark.parametrize("offset", [1, 3, 4, 8, 15])
+def test_misaligned_inputs(length, offset):
+    host = workloads.uniform_bytes(length + 7, length + offset)
+    dev = host.cuda()
+    view = dev[offset:]
+    got = bytes(binding.blake3_keyed_hash(view, KEY).cpu().numpy())
+    assert got == oracle.keyed_hash(host[offset:], KEY)
+
+
+@pytest.mark.parametrize("length", [0, 1, 1024, 1025, 13 * 1024 + 7, 255 * 1024, 256 * 1024, 257 * 1024 - 1,
+                                    600 * 1024 + 9])
+@pytest.mark.parametrize("chunk_offset", [0, 5, 1 << 32])
+def test_chunk_cvs(length, chunk_offset):
+    host = workloads.uniform_bytes(90 + length, length)
+    got = binding.blake3_keyed_chunk_cvs(host.cuda(), KEY, chunk_offset).cpu().numpy()
+    ref = oracle.chunk_cvs(host, KEY, chunk_offset)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("leaves_log2", [5, 6, 7, 8])
+@pytest.mark.parametrize("length", [1024, 31 * 1024 + 1, 64 * 1024, 1000 * 1024 + 1, 2048 * 1024])
+def test_tile_roots(leaves_log2, length):
+    host = workloads.uniform_bytes(7 + length, length)
+    roots = binding.blake3_keyed_tile_roots(host.cuda(), KEY, 0, leaves_log2).cpu().numpy()
+    tile = (1 << leaves_log2) * 1024
+    ntiles = -(-length // tile)
+    assert roots.shape == (ntiles, 32)
+    for i in range(ntiles):
+        ref = oracle.subtree_cv(host[i * tile:(i + 1) * tile], KEY, i << leaves_log2, is_root=False)
+        assert bytes(roots[i]) == ref, i
+
+
+@pytest.mark.parametrize("leaves_log2", [5, 6, 7, 8])
+@pytest.mark.parametrize("group_log2", [1, 2, 3, 5, 10])
+@pytest.mark.parametrize("length", [13 * 1024 + 7, 777 * 1024, 5000 * 1024 + 333])
+def test_digest_independent_of_tile_and_group_size(leaves_log2, group_log2, length):
+    """Page section "Kernel 1": 2^t is free, so the digest must not depend on it."""
+    host = workloads.uniform_bytes(length, length)
+    ref = oracle.keyed_hash(host, KEY)
+    d = host.cuda()
+    tiles = binding.blake3_tile_count(length, leaves_log2)
+    if tiles == 1:
+        roots = binding.blake3_keyed_tile_roots(d, KEY, 0, leaves_log2, is_root=True)
+        got = bytes(roots[0].cpu().numpy())
+    else:
+        roots = binding.blake3_keyed_tile_roots(d, KEY, 0, leaves_log2)
+        got = bytes(binding.blake3_keyed_reduce_cvs(roots, KEY, True, group_log2).cpu().numpy())
+    assert got == ref
+
+
+@pytest.mark.parametrize("count", [1, 2, 3, 13, 32, 33, 100, 1024, 1025, 3000])
+def test_reduce_cvs_against_oracle_tree(count):
+    """Random CVs as leaves: the reduction must build the left-full, left-large tree."""
+    cvs = workloads.uniform_bytes(4242 + count, 32 * count).reshape(count, 32)
+    leaves = [bytes(cvs[i].numpy()) for i in range(count)]
+
+    def fold(xs, is_root):
+        if len(xs) == 1:
+            return xs[0]
+        p = 1
+        while p * 2 < len(xs):
+            p *= 2
+        return oracle.parent_cv(KEY, fold(xs[:p], False), fold(xs[p:], False), is_root)
+
+    for group_log2 in (1, 4, 10):
+        got = bytes(binding.blake3_keyed_reduce_cvs(cvs.cuda(), KEY, count > 1, group_log2).cpu().numpy())
+        assert got == fold(leaves, count > 1), (count, group_log2)
+
+
+@pytest.mark.parametrize("length,chunk_offset", [(1024, 0), (1024, 7), (4 * 1024, 4), (64 * 1024, 64),
+                                                 (1024 * 1024, 1 << 20), (300 * 1024 + 5, 512),
+                                                 (13 * 1024 + 7, 16)])
+@pytest.mark.parametrize("is_root", [False, True])
+def test_subtree_root(length, chunk_offset, is_root):
+    host = workloads.uniform_bytes(length + 11, length)
+    got = bytes(binding.blake3_keyed_subtree_root(host.cuda(), KEY, chunk_offset, is_root).cpu().numpy())
+    assert got == oracle.subtree_cv(host, KEY, chunk_offset, is_root)
+
+
+def test_subtree_roots_compose_to_the_digest():
+    """Two 512-chunk halves hashed as subtrees, then one parent with ROOT == the digest."""
+    length = 1024 * 1024
+    host = workloads.uniform_bytes(31, length)
+    d = host.cuda()
+    left = binding.blake3_keyed_subtree_root(d[:512 * 1024], KEY, 0)
+    right = binding.blake3_keyed_subtree_root(d[512 * 1024:], KEY, 512)
+    top = oracle.parent_cv(KEY, bytes(left.cpu().numpy()), bytes(right.cpu().numpy()), True)
+    assert top == oracle.keyed_hash(host, KEY)
+    with pytest.raises(binding.B3GError):
+        binding.blake3_keyed_subtree_root(d[512 * 1024:], KEY, 256)
+
+
+def test_workspace_variant_and_streams():
+    w = workloads.WORKLOADS["1MiB"]
+    host = w.data()
+    d = host.cuda()
+    ref = oracle.keyed_hash(host, w.key())
+    ws = torch.empty(binding.blake3_workspace_size(d.numel()), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = binding.blake3_keyed_hash_ws(d, w.key(), ws, stream=s)
+    s.synchronize()
+    assert bytes(out.cpu().numpy()) == ref
+    with pytest.raises(binding.B3GError):
+        binding.blake3_keyed_hash_ws(d, w.key(), ws[:16])
+
+
+def test_bf16_matrix_config():
+    w = workloads.WORKLOADS["bf16_256MiB"]
+    host = w.data()
+    assert _gpu_digest(host, w.key()) == oracle.keyed_hash(host, w.key())
+
+
+def test_generator_same_bytes_on_gpu_and_cpu():
+    for seed, n in ((4, 1 << 20), (6, 3 * (1 << 20) + 777)):
+        a = workloads.uniform_bytes(seed, n, device="cuda").cpu()
+        b = workloads.uniform_bytes(seed, n)
+        assert torch.equal(a, b)
