@@ -184,7 +184,7 @@ def run_ours(args):
     build.build()
     lib = binding.library()
 
-    w = workloads.WORKLOADS[WORKLOAD]
+    w = workloads.WORKLOADS[args.workload]
     key = w.key()
     n = w.nbytes
     dev = w.data(device="cuda")
@@ -278,6 +278,40 @@ def run_ours(args):
     roofline["frac_of_min_roofline"] = (n / leaf_s / 1e9) / roofline["roofline_gbs"]
 
     # end to end through the public call, host buffers, copies inside the timed region
+    e2e = None
+    host = None
+    if not args.no_e2e:
+        e2e, host = _e2e(args, binding, dev, key, out, stream, digest_api, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if host is None:
+            host = dev.cpu()
+        sample, dt = _oracle_sample(host, key, args.cpu_seconds)
+        cpu = {"value": sample / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {sample} bytes of the workload hashed as one input by the single-threaded "
+                         f"C oracle ({dt:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": f"{w.name} keyed BLAKE3, {w.kind} bytes seed {w.data_seed}, key seed {w.key_seed}",
+                   "bytes": n, "chunks": nchunks, "leaves_per_cta": 1 << leaves_log2, "cta_roots": tiles,
+                   "l2": f"input {n / 1e9:.2f} GB > 126 MB L2; no flush needed", "parallelism": f"replicas{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches * args.steps, "clocks": clocks,
+        "digest": digest_api.hex(),
+    }
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def _e2e(args, binding, dev, key, out, stream, digest_api, world):
+    n = dev.numel()
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     host = torch.empty(n, dtype=torch.uint8, pin_memory=True)
     host.copy_(dev)
@@ -302,30 +336,7 @@ def run_ours(args):
         raise RuntimeError("end-to-end digest differs")
     e2e = {"value": world * n / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": n,
            "d2h_bytes_per_step": 32, "ms_per_step": e2e_ms, "steps": e2e_steps}
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample, dt = _oracle_sample(host, key, args.cpu_seconds)
-        cpu = {"value": sample / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {sample} bytes of the workload hashed as one input by the single-threaded "
-                         f"C oracle ({dt:.1f} s)"}
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD} keyed BLAKE3, uniform bytes seed 6, key seed 7", "bytes": n,
-                   "chunks": nchunks, "leaves_per_cta": 1 << leaves_log2, "cta_roots": tiles,
-                   "l2": "input 12.9 GB > 126 MB L2; no flush needed", "parallelism": f"replicas{world}"},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches * args.steps, "clocks": clocks,
-        "digest": digest_api.hex(),
-    }
-    if world > 1:
-        torch.distributed.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    return 0
+    return e2e, host
 
 
 def main():
@@ -337,6 +348,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

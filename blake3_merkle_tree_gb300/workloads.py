@@ -20,6 +20,7 @@ Workloads (sizes and seeds):
              (torch CPU generator seeded with 2, float32 rounded to bf16), key seed 3
   4 GiB      2^32 uniform bytes, data seed 4, key seed 5
   12 GiB+777 12,884,902,665 uniform bytes, data seed 6, key seed 7
+  1 GiB      2^30 uniform bytes, data seed 8, key seed 9 (profiling case only)
 """
 
 from __future__ import annotations
@@ -143,6 +144,8 @@ WORKLOADS = {
     "bf16_256MiB": Workload("bf16_256MiB", 8192 * 16384 * 2, 2, 3, kind="bf16"),
     "4GiB": Workload("4GiB", 1 << 32, 4, 5),
     "12GiB+777": Workload("12GiB+777", 12 * (1 << 30) + 777, 6, 7),
+    # profiling case: larger than L2, small enough for a many-pass profiler capture
+    "1GiB": Workload("1GiB", 1 << 30, 8, 9),
 }
 
 RAGGED_KEY_SEED = 1
