@@ -15,6 +15,7 @@ from __future__ import annotations
 _BINDING_NAMES = (
     "blake3_keyed_hash",
     "blake3_keyed_hash_ws",
+    "blake3_keyed_hash_noalloc",
     "blake3_workspace_size",
     "blake3_keyed_chunk_cvs",
     "blake3_keyed_subtree_root",

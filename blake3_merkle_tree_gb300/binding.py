@@ -52,6 +52,7 @@ def library() -> ctypes.CDLL:
             "blake3_keyed_hash": (i32, [vp, u64, vp, vp, vp]),
             "blake3_workspace_size": (sz, [u64]),
             "blake3_keyed_hash_ws": (i32, [vp, u64, vp, vp, vp, sz, vp]),
+            "blake3_keyed_hash_noalloc": (i32, [vp, u64, vp, vp, vp]),
             "blake3_keyed_chunk_cvs": (i32, [vp, u64, u64, vp, vp, vp]),
             "blake3_keyed_subtree_root": (i32, [vp, u64, u64, vp, i32, vp, vp]),
             "blake3_tile_count": (u64, [u64, i32]),
@@ -142,6 +143,16 @@ def blake3_keyed_hash_ws(data: torch.Tensor, key, workspace: torch.Tensor | None
     st = library().blake3_keyed_hash_ws(_dev_ptr(data, "data"), _nbytes(data), _key(key), _dev_ptr(out, "out"),
                                         ws_ptr, ws_bytes, _stream(stream))
     _check(st, "blake3_keyed_hash_ws")
+    return out
+
+
+def blake3_keyed_hash_noalloc(data: torch.Tensor, key, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """The digest without any device allocation: for callers that cannot allocate at
+    hashing time.  Uses the library's fixed scratch array (inputs up to 16 GiB); calls
+    that overlap on the GPU race on that array, so serialise them."""
+    st = library().blake3_keyed_hash_noalloc(_dev_ptr(data, "data"), _nbytes(data), _key(key),
+                                             _dev_ptr(out, "out"), _stream(stream))
+    _check(st, "blake3_keyed_hash_noalloc")
     return out
 
 

@@ -170,6 +170,8 @@ b3g_status hash_range_alloc(const void *d_in, uint64_t len, uint64_t chunk_offse
 
 }  // namespace
 
+b3g_status device_status_word(uint32_t **out) { return status_word(out); }
+
 b3g_status cuda_fail(cudaError_t err, const char *what) {
     std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s (%d)", what, cudaGetErrorString(err),
                   static_cast<int>(err));

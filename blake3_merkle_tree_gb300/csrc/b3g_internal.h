@@ -62,4 +62,7 @@ b3g_status launch_wait_probe(uint64_t limit_ns, int *d_flag, cudaStream_t stream
 // Records a CUDA error for blake3_last_cuda_error() and returns B3G_ERR_CUDA.
 b3g_status cuda_fail(cudaError_t err, const char *what);
 
+// Device address of the current device's status word (looked up once per device).
+b3g_status device_status_word(uint32_t **out);
+
 }  // namespace b3g

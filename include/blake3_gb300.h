@@ -180,6 +180,37 @@ b3g_status blake3_device_status(uint32_t *status_out);
  */
 b3g_status blake3_selftest_bounded_wait(uint32_t limit_us, int *timed_out_out);
 
+/*
+ * blake3_keyed_hash_noalloc -- the same digest as blake3_keyed_hash, computed without
+ * allocating any device memory.  The paper has no counterpart to this entry point.
+ *
+ * For callers that cannot allocate device memory when they hash: for example a
+ * process whose GPU memory is already owned by another allocator (a framework's
+ * caching allocator), a latency-critical loop that cannot accept the device-wide
+ * synchronisation cudaMalloc/cudaFree may cause, or a service that forbids allocation
+ * after start-up.  The CTA roots are kept in a fixed scratch array of 2 MiB + 4 KiB
+ * that is part of the library's device image: every GPU that loads libb3g.so holds it
+ * until the process exits.  The caller still provides the input and the 32-byte,
+ * 16-byte aligned output.
+ *
+ * Limits and rules:
+ *   - len may be at most B3G_NOALLOC_MAX_LEN (16 GiB); a larger input returns
+ *     B3G_ERR_WORKSPACE before anything is launched.
+ *   - The first call on each device looks up the scratch array's device address
+ *     (with that device current) and caches it; make that first call before any
+ *     stream capture on that device.
+ *   - All calls share the one scratch array, and it keeps the last call's contents.
+ *     Calls whose work overlaps on the GPU (concurrent streams, or several host
+ *     threads on one device) race on it and give wrong digests; serialise them.
+ *     Within one call everything read from the scratch is written first, so
+ *     leftovers of an earlier call do no harm.
+ * Errors: B3G_ERR_NULL, B3G_ERR_ALIGN (d_out32), B3G_ERR_WORKSPACE (len too large),
+ * B3G_ERR_CUDA.
+ */
+#define B3G_NOALLOC_MAX_LEN (16ull << 30)
+b3g_status blake3_keyed_hash_noalloc(const void *d_in, uint64_t len, const uint8_t key[32],
+                                     uint8_t *d_out32, b3g_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
