@@ -339,6 +339,90 @@ def _e2e(args, binding, dev, key, out, stream, digest_api, world):
     return e2e, host
 
 
+def _timed(fn, steps, warmup):
+    """Mean milliseconds of fn() over `steps` calls after `warmup`, CUDA events on the current stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_mode(args):
+    """Measurements of the extensions, one JSON line each (not the headline)."""
+    from blake3_merkle_tree_gb300 import binding, build
+
+    torch.cuda.set_device(0)
+    build.build()
+    binding.library()
+    if args.mode == "xof":
+        w = workloads.WORKLOADS["1MiB"]
+        d = w.data(device="cuda")
+        out_len = args.xof_bytes
+        out = torch.empty(out_len, dtype=torch.uint8, device="cuda")
+        ms = _timed(lambda: binding.blake3_keyed_hash_xof(d, w.key(), out_len, out=out), args.steps, args.warmup)
+        line = {"mode": "xof", "metric": "GB/s of extendable output (keyed BLAKE3, 1 GB300)",
+                "value": out_len / ms / 1e6, "unit": "GB/s", "ms_per_call": ms,
+                "config": {"input": "1MiB uniform seed 0, key seed 1", "out_bytes": out_len},
+                "ops_per_output_byte": OPS_PER_COMPRESSION / 64}
+    elif args.mode == "stream":
+        w = workloads.WORKLOADS[args.workload]
+        d = w.data(device="cuda")
+        seg = args.segment_bytes
+        h = binding.Hasher(w.key())
+
+        def run():
+            h.reset()
+            for a in range(0, d.numel(), seg):
+                h.update(d[a:a + seg])
+            h.finalize(out=out32)
+
+        out32 = torch.empty(32, dtype=torch.uint8, device="cuda")
+        ms = _timed(run, args.steps, args.warmup)
+        one = bytes(binding.blake3_keyed_hash(d, w.key()).cpu().numpy())
+        if bytes(out32.cpu().numpy()) != one:
+            raise RuntimeError("streaming digest differs from the one-shot digest")
+        ms_one = _timed(lambda: binding.blake3_keyed_hash(d, w.key(), out=out32), args.steps, args.warmup)
+        line = {"mode": "stream", "metric": "GB/s hashed through the streaming hasher (keyed BLAKE3, 1 GB300)",
+                "value": d.numel() / ms / 1e6, "unit": "GB/s", "ms_per_digest": ms,
+                "one_shot_GBps": d.numel() / ms_one / 1e6,
+                "config": {"workload": w.name, "segment_bytes": seg, "segments": -(-d.numel() // seg)}}
+    else:  # small: the 1 MiB digest, per call and replayed from a CUDA graph
+        w = workloads.WORKLOADS["1MiB"]
+        d = w.data(device="cuda")
+        key = w.key()
+        out32 = torch.empty(32, dtype=torch.uint8, device="cuda")
+        ms_call = _timed(lambda: binding.blake3_keyed_hash(d, key, out=out32), args.steps, args.warmup)
+        ws = torch.empty(max(16, binding.blake3_workspace_size(d.numel())), dtype=torch.uint8, device="cuda")
+        per_graph = 50
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                binding.blake3_keyed_hash_ws(d, key, ws, out=out32)
+        torch.cuda.current_stream().wait_stream(s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for _ in range(per_graph):
+                binding.blake3_keyed_hash_ws(d, key, ws, out=out32)
+        ms_graph = _timed(graph.replay, max(3, args.steps // per_graph), 2) / per_graph
+        if bytes(out32.cpu().numpy()) != bytes(binding.blake3_keyed_hash(d, key).cpu().numpy()):
+            raise RuntimeError("graph-replayed digest differs")
+        line = {"mode": "small", "metric": "GB/s hashed, 1 MiB input (keyed BLAKE3, 1 GB300)",
+                "value": d.numel() / ms_graph / 1e6, "unit": "GB/s", "us_per_digest_graph": ms_graph * 1e3,
+                "us_per_call_eager": ms_call * 1e3, "eager_GBps": d.numel() / ms_call / 1e6,
+                "config": {"workload": "1MiB uniform seed 0, key seed 1",
+                           "graph": f"{per_graph} blake3_keyed_hash_ws calls per CUDA graph"}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -350,11 +434,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--mode", choices=["headline", "xof", "stream", "small"], default="headline")
+    ap.add_argument("--xof-bytes", type=int, default=1 << 32)
+    ap.add_argument("--segment-bytes", type=int, default=(256 << 20) + 777)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode != "headline":
+        return run_mode(args)
     return run_ours(args)
 
 

@@ -16,6 +16,8 @@ _BINDING_NAMES = (
     "blake3_keyed_hash",
     "blake3_keyed_hash_ws",
     "blake3_keyed_hash_noalloc",
+    "blake3_keyed_hash_xof",
+    "Hasher",
     "blake3_workspace_size",
     "blake3_keyed_chunk_cvs",
     "blake3_keyed_subtree_root",

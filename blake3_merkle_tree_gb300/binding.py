@@ -61,6 +61,13 @@ def library() -> ctypes.CDLL:
             "blake3_keyed_reduce_cvs": (i32, [vp, u64, vp, i32, i32, vp, vp, sz, vp]),
             "blake3_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32)]),
             "blake3_selftest_bounded_wait": (i32, [ctypes.c_uint32, ctypes.POINTER(ctypes.c_int)]),
+            "blake3_keyed_hash_xof": (i32, [vp, u64, vp, vp, u64, vp]),
+            "blake3_hasher_new": (i32, [vp, ctypes.POINTER(vp)]),
+            "blake3_hasher_free": (None, [vp]),
+            "blake3_hasher_reset": (i32, [vp]),
+            "blake3_hasher_count": (u64, [vp]),
+            "blake3_hasher_update": (i32, [vp, vp, u64, vp]),
+            "blake3_hasher_finalize": (i32, [vp, vp, u64, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -225,3 +232,56 @@ def blake3_selftest_bounded_wait(limit_us: int) -> bool:
     flag = ctypes.c_int(-1)
     _check(library().blake3_selftest_bounded_wait(limit_us, ctypes.byref(flag)), "blake3_selftest_bounded_wait")
     return flag.value == 1
+
+
+def blake3_keyed_hash_xof(data: torch.Tensor, key, out_len: int, out: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """out_len bytes of extendable output (a uint8 CUDA tensor); the first 32 are the digest."""
+    if out is None:
+        dev = data.device if data.is_cuda else torch.device("cuda")
+        out = torch.empty(out_len, dtype=torch.uint8, device=dev)
+    if _nbytes(out) < out_len:
+        raise ValueError("output too small")
+    st = library().blake3_keyed_hash_xof(_dev_ptr(data, "data"), _nbytes(data), _key(key),
+                                         _dev_ptr(out, "out") if out_len else None, out_len, _stream(stream))
+    _check(st, "blake3_keyed_hash_xof")
+    return out
+
+
+class Hasher:
+    """Streaming keyed hasher over device segments (blake3_hasher_* of the C ABI)."""
+
+    def __init__(self, key):
+        self._h = ctypes.c_void_p()
+        _check(library().blake3_hasher_new(_key(key), ctypes.byref(self._h)), "blake3_hasher_new")
+
+    def update(self, data: torch.Tensor, stream=None) -> "Hasher":
+        _check(library().blake3_hasher_update(self._h, _dev_ptr(data, "data"), _nbytes(data), _stream(stream)),
+               "blake3_hasher_update")
+        return self
+
+    def finalize(self, out_len: int = 32, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty(max(out_len, 1), dtype=torch.uint8, device="cuda")[:out_len]
+        _check(library().blake3_hasher_finalize(self._h, _dev_ptr(out, "out") if out_len else None, out_len,
+                                                _stream(stream)), "blake3_hasher_finalize")
+        return out
+
+    def reset(self) -> "Hasher":
+        _check(library().blake3_hasher_reset(self._h), "blake3_hasher_reset")
+        return self
+
+    @property
+    def count(self) -> int:
+        return int(library().blake3_hasher_count(self._h))
+
+    def close(self) -> None:
+        if self._h:
+            library().blake3_hasher_free(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -19,7 +19,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libb3g.so")
-SOURCES = ["b3g_leaf.cu", "b3g_reduce.cu", "b3g_api.cu", "b3g_noalloc.cu"]
+SOURCES = ["b3g_leaf.cu", "b3g_reduce.cu", "b3g_api.cu", "b3g_noalloc.cu", "b3g_stream.cu"]
 HEADERS = ["b3g_device.cuh", "b3g_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -125,6 +125,22 @@ LeafArgs leaf_args(const void *d_in, uint64_t len, uint64_t chunk_offset, const 
     return a;
 }
 
+// Chunks per CTA subtree (log2) for an input of n chunks.  Large inputs use 256.
+// An input of at most 2^16 chunks (64 MiB) cannot fill the GPU with 256-chunk CTAs,
+// so the subtree shrinks (down to 32 chunks) until there are at least kSpreadTiles
+// CTAs: each chunk is a chain of 16 dependent compressions, so small inputs finish
+// sooner with fewer warps per SM.  A function of n alone, so that the workspace size
+// is a function of the length alone.
+constexpr uint64_t kSmallInputChunks = 1ull << 16;
+constexpr uint64_t kSpreadTiles = 152;
+
+int choose_leaves_log2(uint64_t n_chunks) {
+    int t = kDefaultLeavesLog2;
+    if (n_chunks <= kSmallInputChunks)
+        while (t > kMinLeavesLog2 && ceil_div(n_chunks, 1ull << t) < kSpreadTiles) --t;
+    return t;
+}
+
 // The whole path: leaf kernel, then the reduction levels.  `ws` must hold
 // blake3_workspace_size(len) bytes when more than one tile exists.
 b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32], bool root,
@@ -132,7 +148,7 @@ b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, con
     uint32_t *status = nullptr;
     b3g_status st = status_word(&status);
     if (st != B3G_OK) return st;
-    const int t = kDefaultLeavesLog2;
+    const int t = choose_leaves_log2(n_chunks_of(len));
     LeafArgs a = leaf_args(d_in, len, chunk_offset, key, t, root, nullptr, status);
     if (a.n_tiles == 1) {
         a.out = d_out32;
@@ -146,7 +162,8 @@ b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, con
 }
 
 size_t hash_workspace(uint64_t len) {
-    const uint64_t tiles = ceil_div(n_chunks_of(len), 1ull << kDefaultLeavesLog2);
+    const uint64_t n = n_chunks_of(len);
+    const uint64_t tiles = ceil_div(n, 1ull << choose_leaves_log2(n));
     if (tiles == 1) return 0;
     return round16(tiles * 32) + reduce_ws(tiles, kDefaultGroupLog2);
 }
@@ -171,6 +188,11 @@ b3g_status hash_range_alloc(const void *d_in, uint64_t len, uint64_t chunk_offse
 }  // namespace
 
 b3g_status device_status_word(uint32_t **out) { return status_word(out); }
+
+b3g_status hash_range_ws(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32], bool root,
+                         uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
+    return hash_range(d_in, len, chunk_offset, key, root, d_out32, ws, stream);
+}
 
 b3g_status cuda_fail(cudaError_t err, const char *what) {
     std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s (%d)", what, cudaGetErrorString(err),

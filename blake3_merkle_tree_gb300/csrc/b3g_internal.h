@@ -65,4 +65,10 @@ b3g_status cuda_fail(cudaError_t err, const char *what);
 // Device address of the current device's status word (looked up once per device).
 b3g_status device_status_word(uint32_t **out);
 
+// The CV of the subtree made of the chunks of d_in[0..len) whose first chunk has global
+// index chunk_offset (ROOT on the final compression if root), written to d_out32;
+// ws holds blake3_workspace_size(len) bytes.
+b3g_status hash_range_ws(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32], bool root,
+                         uint8_t *d_out32, uint8_t *ws, cudaStream_t stream);
+
 }  // namespace b3g

@@ -44,11 +44,18 @@ namespace b3g {
 constexpr uint32_t kBarTree = 1;  // named barrier id of the consumer threads
 
 // ---------------------------------------------------------------------------------
-// Bulk-tensor-copy (TMA) pipeline kernel.
+// Bulk-tensor-copy (TMA) pipeline kernel, warp specialised:
+//   warps 0 .. C/32-1   consumers: one chunk per thread, 16 chained compressions
+//   warp  C/32          producer: one lane issues the bulk tensor copies
+//   warp  C/32+1        reducer: reduces each tile's C chunk CVs to the tile CV
+// The consumers hand their chunk CVs to the reducer through two node buffers
+// (tile k uses buffer k&1) guarded by mbarriers, so a consumer never waits for the
+// tree of the previous tile: it stores its CV, arrives, and starts the next tile.
+//
 //   C          consumers = chunks per tile (2^t), a multiple of 32, at most 256
 //   S          stages in the shared-memory ring
 //   LOAD       bytes of every chunk brought by one load (128 or 64)
-//   CHUNK_CVS  write every chunk CV instead of reducing the tile
+//   CHUNK_CVS  write every chunk CV instead of reducing the tile (no reducer work)
 // ---------------------------------------------------------------------------------
 template <int C, int S, int LOAD, bool CHUNK_CVS>
 struct TmaCfg {
@@ -58,27 +65,36 @@ struct TmaCfg {
     static constexpr int kBlocksPerLoad = LOAD / 64;
     static constexpr uint32_t kStageBytes = C * LOAD;
     static constexpr int kConsumerWarps = C / 32;
-    static constexpr int kThreads = C + 32;
-    static constexpr uint32_t kNodeBytes = C * 32;
-    // stages (1024-aligned for the swizzle), nodes, then 2*S barriers
-    static constexpr size_t kSmemBytes = 1024 + size_t(S) * kStageBytes + kNodeBytes + 16 * S;
-    // The single node buffer is reused tile after tile.  A consumer warp can only
-    // run ahead of the slowest one by S loads, so with S < kLoadsPerTile no warp
-    // can reach the next tile's node stores while warp 0 still reads the previous
-    // tile's nodes (block_tree also ends with a barrier after that read).
-    static_assert(S >= 2 && S < kLoadsPerTile, "stage count");
+    static constexpr int kProducerWarp = kConsumerWarps;
+    static constexpr int kReducerWarp = kConsumerWarps + 1;
+    static constexpr int kThreads = C + 64;
+    static constexpr uint32_t kNodeBytes = C * 32;                  // one node buffer
+    static constexpr uint32_t kScratch1Bytes = (C / 2) * 32;        // odd tree levels
+    static constexpr uint32_t kScratch2Bytes = (C / 4 < 1 ? 1 : C / 4) * 32;  // even levels
+    // layout: [align 1024][S stages][2 node buffers][scratch 1][scratch 2][barriers]
+    static constexpr uint32_t kOffNodes = S * kStageBytes;
+    static constexpr uint32_t kOffScratch1 = kOffNodes + 2 * kNodeBytes;
+    static constexpr uint32_t kOffScratch2 = kOffScratch1 + kScratch1Bytes;
+    static constexpr uint32_t kOffBars = kOffScratch2 + kScratch2Bytes;
+    static constexpr uint32_t kNumBars = 2 * S + 4;
+    static constexpr size_t kSmemBytes = 1024 + size_t(kOffBars) + 8 * kNumBars;
+    static_assert(S >= 2, "stage count");
 };
 
 template <int C, int S, int LOAD, bool CHUNK_CVS>
-__global__ void __launch_bounds__(C + 32)
+__global__ void __launch_bounds__(C + 64)
     leaf_tma_kernel(const __grid_constant__ CUtensorMap tmap, const LeafArgs a) {
     using Cfg = TmaCfg<C, S, LOAD, CHUNK_CVS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t stage0 = (raw + 1023u) & ~1023u;
-    const uint32_t nodes = stage0 + S * Cfg::kStageBytes;
-    const uint32_t full0 = nodes + Cfg::kNodeBytes;  // S barriers, 8 bytes each
-    const uint32_t empty0 = full0 + 8 * S;
+    const uint32_t nodes0 = stage0 + Cfg::kOffNodes;  // buffer b at nodes0 + b * kNodeBytes
+    const uint32_t scratch1 = stage0 + Cfg::kOffScratch1;
+    const uint32_t scratch2 = stage0 + Cfg::kOffScratch2;
+    const uint32_t full0 = stage0 + Cfg::kOffBars;  // S barriers, 8 bytes each
+    const uint32_t empty0 = full0 + 8 * S;          // S barriers
+    const uint32_t cvfull0 = empty0 + 8 * S;        // 2 barriers: node buffer b is filled
+    const uint32_t cvempty0 = cvfull0 + 16;         // 2 barriers: node buffer b is free
 
     const uint32_t tid = threadIdx.x;
     const uint32_t warp = tid >> 5;
@@ -90,11 +106,15 @@ __global__ void __launch_bounds__(C + 32)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, Cfg::kConsumerWarps);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(cvfull0 + 8 * b, C);
+            mbar_init(cvempty0 + 8 * b, 32);
+        }
         fence_mbar_init();
     }
     __syncthreads();
 
-    if (warp == Cfg::kConsumerWarps) {
+    if (warp == Cfg::kProducerWarp) {
         // ------------------------------- producer -------------------------------
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap) : "memory");
@@ -126,18 +146,73 @@ __global__ void __launch_bounds__(C + 32)
         return;
     }
 
-    // --------------------------------- consumers ---------------------------------
     uint32_t key[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) key[i] = a.key[i];
+
+    if (warp == Cfg::kReducerWarp) {
+        // -------------------------------- reducer --------------------------------
+        if constexpr (!CHUNK_CVS) {
+            uint32_t k = 0;
+            for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
+                const uint32_t b = k & 1u;
+                const uint32_t src0 = nodes0 + b * Cfg::kNodeBytes;
+                if (!mbar_wait_bounded(cvfull0 + 8 * b, (k >> 1) & 1u, a.wait_limit_ns)) {
+                    atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
+                    break;
+                }
+                const uint64_t rem = a.n_chunks - tile * C;
+                uint32_t cnt = rem < C ? static_cast<uint32_t>(rem) : static_cast<uint32_t>(C);
+                uint32_t src = src0;
+                uint32_t level = 0;
+                // Levels with more than 32 nodes: pairs (2j, 2j+1) -> node j, lanes
+                // striding over j, ping-ponging between two scratch buffers; an odd
+                // last node moves up unchanged.
+                while (cnt > 32) {
+                    const uint32_t dst = (level & 1u) ? scratch2 : scratch1;
+                    const uint32_t half = cnt >> 1;
+                    for (uint32_t j = lane; j < half; j += 32) {
+                        uint32_t l[8], r[8], p[8];
+                        load_node(src, 2 * j, l);
+                        load_node(src, 2 * j + 1, r);
+                        parent(key, l, r, false, p);
+                        store_node(dst, j, p);
+                    }
+                    if ((cnt & 1u) && lane == 0) {
+                        uint32_t t[8];
+                        load_node(src, cnt - 1, t);
+                        store_node(dst, half, t);
+                    }
+                    __syncwarp();
+                    if (level == 0) mbar_arrive(cvempty0 + 8 * b);  // node buffer read
+                    src = dst;
+                    cnt = (cnt + 1) >> 1;
+                    ++level;
+                }
+                uint32_t x[8];
+                if (lane < cnt) load_node(src, lane, x);
+                __syncwarp();
+                if (level == 0) mbar_arrive(cvempty0 + 8 * b);
+                warp_tree(x, cnt, key, a.root && a.n_tiles == 1);
+                if (lane == 0) {
+                    uint4 *o = reinterpret_cast<uint4 *>(a.out + tile * 32);
+                    o[0] = make_uint4(x[0], x[1], x[2], x[3]);
+                    o[1] = make_uint4(x[4], x[5], x[6], x[7]);
+                }
+            }
+        }
+        return;
+    }
+
+    // --------------------------------- consumers ---------------------------------
     const uint32_t r = tid;
     // 16-byte unit u of this thread's row sits at u ^ swz (TMA 128B / 64B swizzle)
     const uint32_t swz = LOAD == 128 ? (r & 7u) : ((r >> 1) & 3u);
     const uint32_t row_off = r * LOAD;
     uint32_t it = 0;
-    bool aborted = false;
+    uint32_t k = 0;
 
-    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x) {
+    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
         const uint64_t chunk = tile * C + r;
         const bool valid = chunk < a.n_chunks;
         const bool is_tail = a.tail_bytes != 0 && chunk == a.n_full;
@@ -152,15 +227,15 @@ __global__ void __launch_bounds__(C + 32)
 #pragma unroll
         for (int i = 0; i < 8; ++i) cv[i] = key[i];
 
+        bool aborted = false;
 #pragma unroll 1
         for (int ld = 0; ld < Cfg::kLoadsPerTile; ++ld, ++it) {
             const uint32_t s = it % S;
-            const uint32_t k = it / S;
-            if (aborted) continue;
-            if (!mbar_wait_bounded(full0 + 8 * s, k & 1u, a.wait_limit_ns)) {
+            const uint32_t kk = it / S;
+            if (!mbar_wait_bounded(full0 + 8 * s, kk & 1u, a.wait_limit_ns)) {
                 atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
                 aborted = true;
-                continue;
+                break;
             }
             const uint32_t rowp = stage0 + s * Cfg::kStageBytes + row_off;
 #pragma unroll
@@ -187,27 +262,24 @@ __global__ void __launch_bounds__(C + 32)
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * s);
         }
+        if (aborted) break;
 
         if constexpr (CHUNK_CVS) {
-            if (aborted) break;
             if (valid) {
                 uint4 *o = reinterpret_cast<uint4 *>(a.out + chunk * 32);
                 o[0] = make_uint4(cv[0], cv[1], cv[2], cv[3]);
                 o[1] = make_uint4(cv[4], cv[5], cv[6], cv[7]);
             }
         } else {
-            if (valid) store_node(nodes, r, cv);
-            // barrier before the tree; also makes the abort decision uniform
-            if (named_bar_or(kBarTree, C, aborted)) break;
-            const uint64_t rem = a.n_chunks - tile * C;
-            const uint32_t cnt = rem < C ? static_cast<uint32_t>(rem) : static_cast<uint32_t>(C);
-            uint32_t root_cv[8];
-            block_tree(nodes, cnt, r, C, kBarTree, key, a.root && a.n_tiles == 1, root_cv);
-            if (r == 0) {
-                uint4 *o = reinterpret_cast<uint4 *>(a.out + tile * 32);
-                o[0] = make_uint4(root_cv[0], root_cv[1], root_cv[2], root_cv[3]);
-                o[1] = make_uint4(root_cv[4], root_cv[5], root_cv[6], root_cv[7]);
+            // hand the chunk CV to the reducer: wait until node buffer k&1 is free
+            // (the reducer has read tile k-2), store, arrive
+            const uint32_t b = k & 1u;
+            if (k >= 2 && !mbar_wait_bounded(cvempty0 + 8 * b, ((k >> 1) - 1) & 1u, a.wait_limit_ns)) {
+                atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
+                break;
             }
+            if (valid) store_node(nodes0 + b * Cfg::kNodeBytes, r, cv);
+            mbar_arrive(cvfull0 + 8 * b);
         }
     }
 }
@@ -279,20 +351,39 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Stage count and load width per tile size (chosen by measurement on GB300).
+// Stage count and load width per tile size (chosen by measurement on GB300; the
+// B3G_TUNE_* macros exist so that other settings can be built for comparison).
+#ifndef B3G_TUNE_S256
+#define B3G_TUNE_S256 3
+#endif
+#ifndef B3G_TUNE_LOAD256
+#define B3G_TUNE_LOAD256 64
+#endif
+#ifndef B3G_TUNE_S128
+#define B3G_TUNE_S128 4
+#endif
+#ifndef B3G_TUNE_LOAD128
+#define B3G_TUNE_LOAD128 64
+#endif
 template <int C>
 struct Tuning;
 template <>
 struct Tuning<256> {
-    static constexpr int S = 3, LOAD = 128;
+    static constexpr int S = B3G_TUNE_S256, LOAD = B3G_TUNE_LOAD256;
 };
 template <>
 struct Tuning<128> {
-    static constexpr int S = 4, LOAD = 128;
+    static constexpr int S = B3G_TUNE_S128, LOAD = B3G_TUNE_LOAD128;
 };
+#ifndef B3G_TUNE_S64
+#define B3G_TUNE_S64 4
+#endif
+#ifndef B3G_TUNE_LOAD64
+#define B3G_TUNE_LOAD64 64
+#endif
 template <>
 struct Tuning<64> {
-    static constexpr int S = 4, LOAD = 128;
+    static constexpr int S = B3G_TUNE_S64, LOAD = B3G_TUNE_LOAD64;
 };
 template <>
 struct Tuning<32> {

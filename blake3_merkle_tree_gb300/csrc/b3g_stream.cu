@@ -1,0 +1,491 @@
+// b3g_stream.cu -- extendable output and the streaming (segmented) hasher.
+//
+// Source page: "BLAKE3 GPU 400x faster hashing" (qfminer.top).
+//   section "未来工作": the extendable-output mode (XOF) is listed as not implemented.
+//   section "BLAKE3": the tree rules (left subtree full, left subtree at least as
+//     large), which decide when chaining values may be merged.
+// The output mode follows the BLAKE3 specification (O'Connor et al., 2020, section
+// 2.6): the root compression is kept as its inputs, and output block i (64 bytes) is
+// that compression with ROOT set and the counter equal to i.
+//
+// Extendable output: the root's inputs ("root record": CV, message block, block
+// length, flags) are produced on the device, then xof_kernel writes every output
+// block in parallel, one thread per 64-byte block.
+//   - one chunk: the record is the chunk's last block, the CV chained through the
+//     blocks before it;
+//   - several chunks: the record is the top parent, whose children are the largest
+//     power-of-two left subtree and the rest; both are ordinary subtree roots.
+//
+// Streaming hasher: input arrives in device segments of any length.  A small device
+// state holds a stack of subtree CVs and the bytes of an unfinished chunk; the host
+// tracks the counts.
+//   - Every complete chunk is pushed, except while the input is at most one chunk
+//     (that chunk may turn out to be the whole input and then needs ROOT).
+//   - Whole runs of chunks are pushed as aligned power-of-two subtrees computed by
+//     the ordinary leaf and reduction kernels; a subtree pushed at position 0 is
+//     pushed as its two halves, so that the root's two children always exist.
+//   - Before pushing at chunk position p the stack is merged down to popcount(p)
+//     entries (the binary decomposition of p), so merges happen only once it is
+//     known that more input follows.
+//   - Finalize works on a copy of the stack: the unfinished chunk is appended, the
+//     copy is merged down to max(2, popcount(n)) entries and folded right to left;
+//     the bottom entry and the fold are the root's children.  The hasher can keep
+//     absorbing input afterwards.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "b3g_device.cuh"
+#include "b3g_internal.h"
+
+namespace b3g {
+namespace {
+
+constexpr int kStackSlots = 66;
+// device state of a hasher: [stack 66 x 32 B][chunk buffer 1024 B][root record 128 B]
+constexpr size_t kStackBytes = kStackSlots * 32;
+constexpr size_t kBufOff = kStackBytes;
+constexpr size_t kRecordOff = kBufOff + 1024;
+constexpr size_t kStateBytes = kRecordOff + 128;
+// root record words: cv[0..7], block[8..23], block_len[24], flags[25] (ROOT not set)
+constexpr int kRecWords = 26;
+
+// Root record of one chunk of `len` (0..1024) bytes at `p`, with counter ctr.
+__device__ void chunk_record(const uint8_t *p, uint32_t len, uint64_t ctr, const uint32_t key[8],
+                             uint32_t *rec) {
+    const uint32_t nblocks = len == 0 ? 1u : (len + 63u) / 64u;
+    uint32_t cv[8];
+    for (int i = 0; i < 8; ++i) cv[i] = key[i];
+    uint32_t m[16];
+    for (uint32_t b = 0; b + 1 < nblocks; ++b) {
+        load_block_global(p, len, 64ull * b, m);
+        compress(cv, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32), 64u,
+                 kKeyedHash | (b == 0 ? kChunkStart : 0u));
+    }
+    const uint32_t b = nblocks - 1;
+    load_block_global(p, len, 64ull * b, m);
+    for (int i = 0; i < 8; ++i) rec[i] = cv[i];
+    for (int i = 0; i < 16; ++i) rec[8 + i] = m[i];
+    rec[24] = len - 64u * b;
+    rec[25] = kKeyedHash | kChunkEnd | (b == 0 ? kChunkStart : 0u);
+}
+
+// CV (no ROOT) of one chunk.
+__device__ void chunk_cv(const uint8_t *p, uint32_t len, uint64_t ctr, const uint32_t key[8],
+                         uint32_t cv[8]) {
+    uint32_t r[kRecWords];
+    chunk_record(p, len, ctr, key, r);
+    uint32_t m[16];
+    for (int i = 0; i < 8; ++i) cv[i] = r[i];
+    for (int i = 0; i < 16; ++i) m[i] = r[8 + i];
+    compress(cv, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32), r[24], r[25]);
+}
+
+// Merge the top of a stack of CVs (8 words each) down to `target` entries.
+__device__ uint32_t merge_down(uint32_t *st, uint32_t depth, uint32_t target, const uint32_t key[8]) {
+    while (depth > target) {
+        uint32_t l[8], r[8], p[8];
+        for (int i = 0; i < 8; ++i) {
+            l[i] = st[8 * (depth - 2) + i];
+            r[i] = st[8 * (depth - 1) + i];
+        }
+        parent(key, l, r, false, p);
+        for (int i = 0; i < 8; ++i) st[8 * (depth - 2) + i] = p[i];
+        --depth;
+    }
+    return depth;
+}
+
+enum RecordMode : uint32_t {
+    kRecChunk = 0,     // root record of the single chunk at `in`
+    kRecPush = 1,      // merge the stack to `target`, push the CV of the buffered full chunk
+    kRecFinalize = 2,  // root record of the whole input (stack untouched)
+    kRecMerge = 3,     // merge the stack to `target`
+    kRecParent = 4,    // record = (key, message words already in place, 64, KEYED_HASH|PARENT)
+};
+
+struct RecordArgs {
+    const uint8_t *in;  // kRecChunk: the chunk bytes
+    uint8_t *state;     // hasher state, or a scratch area laid out the same way
+    uint64_t pushed;    // chunks whose CVs are in the stack (= counter of the next chunk)
+    uint32_t len;       // bytes of the chunk to finish (kRecChunk, kRecPush, kRecFinalize)
+    uint32_t depth;     // stack entries
+    uint32_t target;    // stack entries after merging (kRecPush, kRecMerge)
+    uint32_t mode;
+    uint32_t key[8];
+};
+
+// The sequential bookkeeping of the hasher on one thread: at most 65 merges and one
+// chunk per launch.
+__global__ void record_kernel(const RecordArgs a) {
+    if (threadIdx.x != 0) return;
+    uint32_t key[8];
+    for (int i = 0; i < 8; ++i) key[i] = a.key[i];
+    uint32_t *stack = reinterpret_cast<uint32_t *>(a.state);
+    uint32_t *rec = reinterpret_cast<uint32_t *>(a.state + kRecordOff);
+    const uint8_t *buf = a.state + kBufOff;
+    switch (a.mode) {
+        case kRecChunk:
+            chunk_record(a.in, a.len, a.pushed, key, rec);
+            return;
+        case kRecMerge:
+            merge_down(stack, a.depth, a.target, key);
+            return;
+        case kRecPush: {
+            const uint32_t d = merge_down(stack, a.depth, a.target, key);
+            uint32_t cv[8];
+            chunk_cv(buf, 1024u, a.pushed, key, cv);
+            for (int i = 0; i < 8; ++i) stack[8 * d + i] = cv[i];
+            return;
+        }
+        case kRecParent:
+            for (int i = 0; i < 8; ++i) rec[i] = key[i];
+            rec[24] = kBlockLen;
+            rec[25] = kKeyedHash | kParent;
+            return;
+        case kRecFinalize: {
+            uint32_t st[kStackSlots * 8];  // a private copy: the hasher state is not changed
+            for (uint32_t i = 0; i < 8 * a.depth; ++i) st[i] = stack[i];
+            uint32_t d = a.depth;
+            uint64_t n = a.pushed;
+            if (a.len > 0) {  // the unfinished chunk becomes the last leaf
+                d = merge_down(st, d, static_cast<uint32_t>(__popcll(n)), key);
+                chunk_cv(buf, a.len, n, key, st + 8 * d);
+                ++d;
+                ++n;
+            }
+            const uint32_t pc = static_cast<uint32_t>(__popcll(n));
+            d = merge_down(st, d, pc < 2 ? 2u : pc, key);
+            uint32_t cv[8];
+            for (int i = 0; i < 8; ++i) cv[i] = st[8 * (d - 1) + i];
+            for (uint32_t e = d - 1; e > 1; --e) {
+                uint32_t l[8];
+                for (int i = 0; i < 8; ++i) l[i] = st[8 * (e - 1) + i];
+                parent(key, l, cv, false, cv);
+            }
+            for (int i = 0; i < 8; ++i) {
+                rec[i] = key[i];
+                rec[8 + i] = st[i];
+                rec[16 + i] = cv[i];
+            }
+            rec[24] = kBlockLen;
+            rec[25] = kKeyedHash | kParent;
+            return;
+        }
+        default:
+            return;
+    }
+}
+
+struct XofArgs {
+    const uint32_t *rec;  // root record (device)
+    uint8_t *out;
+    uint64_t out_len;
+};
+
+// Output block i = the root compression with counter i and ROOT, 64 bytes.
+__global__ void __launch_bounds__(256) xof_kernel(const XofArgs a) {
+    const uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i * 64 >= a.out_len) return;
+    uint32_t cv[8], m[16], o[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) cv[k] = __ldg(a.rec + k);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) m[k] = __ldg(a.rec + 8 + k);
+    const uint32_t blen = __ldg(a.rec + 24);
+    const uint32_t flags = __ldg(a.rec + 25) | kRoot;
+    compress_full(cv, m, static_cast<uint32_t>(i), static_cast<uint32_t>(i >> 32), blen, flags, o);
+    uint8_t *dst = a.out + i * 64;
+    const uint64_t rest = a.out_len - i * 64;
+    if (rest >= 64 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        return;
+    }
+    const uint32_t take = rest < 64 ? static_cast<uint32_t>(rest) : 64u;
+#pragma unroll
+    for (uint32_t k = 0; k < 64; ++k)
+        if (k < take) dst[k] = static_cast<uint8_t>(o[k >> 2] >> (8 * (k & 3)));
+}
+
+b3g_status launch_record(const RecordArgs &a, cudaStream_t s) {
+    record_kernel<<<1, 32, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "record_kernel launch");
+}
+
+b3g_status launch_xof(const uint32_t *rec, uint8_t *out, uint64_t out_len, cudaStream_t s) {
+    if (out_len == 0) return B3G_OK;
+    const uint64_t blocks = (out_len + 63) / 64;
+    const uint64_t grid = (blocks + 255) / 256;
+    if (grid > 0x7fffffffull) return B3G_ERR_ARG;
+    XofArgs xa{rec, out, out_len};
+    xof_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(xa);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "xof_kernel launch");
+}
+
+uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+
+uint32_t popcount64(uint64_t x) { return static_cast<uint32_t>(__builtin_popcountll(x)); }
+
+void key_words(const uint8_t key[32], uint32_t out[8]) {
+    for (int i = 0; i < 8; ++i)
+        out[i] = static_cast<uint32_t>(key[4 * i]) | (static_cast<uint32_t>(key[4 * i + 1]) << 8) |
+                 (static_cast<uint32_t>(key[4 * i + 2]) << 16) | (static_cast<uint32_t>(key[4 * i + 3]) << 24);
+}
+
+RecordArgs record_args(uint8_t *state, const uint32_t key[8], uint32_t mode) {
+    RecordArgs ra;
+    std::memset(&ra, 0, sizeof ra);
+    ra.state = state;
+    std::memcpy(ra.key, key, sizeof ra.key);
+    ra.mode = mode;
+    return ra;
+}
+
+b3g_status check_device(int want) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    return dev == want ? B3G_OK : B3G_ERR_ARG;
+}
+
+}  // namespace
+}  // namespace b3g
+
+using namespace b3g;
+
+// Host object of a streaming hasher (opaque to callers).
+struct b3g_hasher {
+    uint8_t key[32];
+    uint32_t kw[8];
+    uint8_t *state;    // device: stack, chunk buffer, root record
+    int device;
+    uint64_t count;    // bytes absorbed
+    uint64_t pushed;   // chunks whose CVs are represented in the stack
+    uint32_t depth;    // stack entries
+    uint32_t buf_len;  // bytes of the unfinished chunk in the buffer
+};
+
+namespace {
+
+// Push the chunks [h->pushed, h->pushed + nchunks) that start at `p` as aligned
+// power-of-two subtrees.
+b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStream_t s) {
+    struct Piece {
+        uint64_t pos, size;
+    };
+    std::vector<Piece> pieces;
+    uint64_t pos = h->pushed, left = nchunks;
+    while (left > 0) {
+        uint64_t size = 1;
+        while (size * 2 <= left && (pos == 0 || (pos % (size * 2)) == 0)) size *= 2;
+        if (pos == 0 && size >= 2) {  // keep the halves of a subtree starting at 0
+            pieces.push_back({0, size / 2});
+            pieces.push_back({size / 2, size / 2});
+        } else {
+            pieces.push_back({pos, size});
+        }
+        pos += size;
+        left -= size;
+    }
+    uint64_t biggest = 0;
+    for (const Piece &pc : pieces) biggest = pc.size > biggest ? pc.size : biggest;
+    const size_t ws_bytes = blake3_workspace_size(biggest * kChunkBytes);
+    uint8_t *ws = nullptr;
+    if (ws_bytes) {
+        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), ws_bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
+    }
+    b3g_status st = B3G_OK;
+    const uint64_t base = h->pushed;
+    for (const Piece &pc : pieces) {
+        const uint32_t target = popcount64(pc.pos);
+        if (h->depth > target) {
+            RecordArgs ra = record_args(h->state, h->kw, kRecMerge);
+            ra.depth = h->depth;
+            ra.target = target;
+            st = launch_record(ra, s);
+            if (st != B3G_OK) break;
+            h->depth = target;
+        }
+        if (h->depth >= kStackSlots) {
+            st = B3G_ERR_ARG;
+            break;
+        }
+        st = hash_range_ws(p + (pc.pos - base) * kChunkBytes, pc.size * kChunkBytes, pc.pos, h->key, false,
+                           h->state + 32ull * h->depth, ws, s);
+        if (st != B3G_OK) break;
+        h->depth += 1;
+        h->pushed = pc.pos + pc.size;
+    }
+    if (ws) {
+        cudaError_t e = cudaFreeAsync(ws, s);
+        if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
+    }
+    return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+b3g_status blake3_keyed_hash_xof(const void *d_in, uint64_t len, const uint8_t key[32], uint8_t *d_out,
+                                 uint64_t out_len, b3g_stream_t stream) {
+    if (!key || (!d_out && out_len > 0) || (!d_in && len > 0)) return B3G_ERR_NULL;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t kw[8];
+    key_words(key, kw);
+    const uint64_t n = len == 0 ? 1 : ceil_div(len, kChunkBytes);
+    uint64_t left_n = 1;
+    while (n > 1 && left_n * 2 < n) left_n *= 2;
+    const uint64_t left_bytes = left_n * kChunkBytes;
+    // scratch: a state-shaped area for the record, then the two subtree workspaces
+    const size_t ws_left = n > 1 ? blake3_workspace_size(left_bytes) : 0;
+    const size_t ws_right = n > 1 ? blake3_workspace_size(len - left_bytes) : 0;
+    const size_t off1 = (kStateBytes + 255) & ~size_t(255);
+    const size_t off2 = off1 + ((ws_left + 255) & ~size_t(255));
+    uint8_t *scratch = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), off2 + ws_right, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
+    uint32_t *rec = reinterpret_cast<uint32_t *>(scratch + kRecordOff);
+    b3g_status st;
+    if (n == 1) {
+        RecordArgs ra = record_args(scratch, kw, kRecChunk);
+        ra.in = static_cast<const uint8_t *>(d_in);
+        ra.len = static_cast<uint32_t>(len);
+        st = launch_record(ra, s);
+    } else {
+        // the root's children, written straight into the record's message words
+        st = hash_range_ws(d_in, left_bytes, 0, key, false, reinterpret_cast<uint8_t *>(rec + 8), scratch + off1,
+                           s);
+        if (st == B3G_OK)
+            st = hash_range_ws(static_cast<const uint8_t *>(d_in) + left_bytes, len - left_bytes, left_n, key, false,
+                               reinterpret_cast<uint8_t *>(rec + 16), scratch + off2, s);
+        if (st == B3G_OK) st = launch_record(record_args(scratch, kw, kRecParent), s);
+    }
+    if (st == B3G_OK) st = launch_xof(rec, d_out, out_len, s);
+    e = cudaFreeAsync(scratch, s);
+    if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
+    return st;
+}
+
+b3g_status blake3_hasher_new(const uint8_t key[32], b3g_hasher **out) {
+    if (!key || !out) return B3G_ERR_NULL;
+    *out = nullptr;
+    b3g_hasher *h = new (std::nothrow) b3g_hasher;
+    if (!h) return B3G_ERR_ARG;
+    std::memcpy(h->key, key, 32);
+    key_words(key, h->kw);
+    h->count = h->pushed = 0;
+    h->depth = h->buf_len = 0;
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void **>(&h->state), kStateBytes);
+    if (e != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "blake3_hasher_new");
+    }
+    *out = h;
+    return B3G_OK;
+}
+
+void blake3_hasher_free(b3g_hasher *h) {
+    if (!h) return;
+    int prev = -1;
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != h->device) cudaSetDevice(h->device);
+    cudaFree(h->state);
+    if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
+    delete h;
+}
+
+b3g_status blake3_hasher_reset(b3g_hasher *h) {
+    if (!h) return B3G_ERR_NULL;
+    h->count = h->pushed = 0;
+    h->depth = h->buf_len = 0;
+    return B3G_OK;
+}
+
+uint64_t blake3_hasher_count(const b3g_hasher *h) { return h ? h->count : 0; }
+
+b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b3g_stream_t stream) {
+    if (!h || (!d_in && len > 0)) return B3G_ERR_NULL;
+    if (len == 0) return B3G_OK;
+    b3g_status st = check_device(h->device);
+    if (st != B3G_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint8_t *p = static_cast<const uint8_t *>(d_in);
+    uint8_t *buf = h->state + kBufOff;
+    cudaError_t e;
+    // at most one chunk in total: keep the bytes, it may be the whole input
+    if (h->count + len <= kChunkBytes) {
+        e = cudaMemcpyAsync(buf + h->buf_len, p, len, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+        h->buf_len += static_cast<uint32_t>(len);
+        h->count += len;
+        return B3G_OK;
+    }
+    uint64_t rest = len;
+    // complete the buffered chunk, and push it once it is full
+    if (h->buf_len > 0) {
+        const uint64_t fill = kChunkBytes - h->buf_len < rest ? kChunkBytes - h->buf_len : rest;
+        if (fill) {
+            e = cudaMemcpyAsync(buf + h->buf_len, p, fill, cudaMemcpyDeviceToDevice, s);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+        }
+        h->buf_len += static_cast<uint32_t>(fill);
+        p += fill;
+        rest -= fill;
+        h->count += fill;
+        if (h->buf_len < kChunkBytes) return B3G_OK;
+        RecordArgs ra = record_args(h->state, h->kw, kRecPush);
+        ra.depth = h->depth;
+        ra.target = popcount64(h->pushed);
+        ra.pushed = h->pushed;
+        st = launch_record(ra, s);
+        if (st != B3G_OK) return st;
+        h->depth = ra.target + 1;
+        h->pushed += 1;
+        h->buf_len = 0;
+    }
+    // whole chunks, then the unfinished tail into the buffer
+    const uint64_t full = rest / kChunkBytes;
+    if (full) {
+        st = push_run(h, p, full, s);
+        if (st != B3G_OK) return st;
+    }
+    const uint64_t tail = rest - full * kChunkBytes;
+    if (tail) {
+        e = cudaMemcpyAsync(buf, p + full * kChunkBytes, tail, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+    }
+    h->buf_len = static_cast<uint32_t>(tail);
+    h->count += rest;
+    return B3G_OK;
+}
+
+b3g_status blake3_hasher_finalize(const b3g_hasher *h, uint8_t *d_out, uint64_t out_len, b3g_stream_t stream) {
+    if (!h || (!d_out && out_len > 0)) return B3G_ERR_NULL;
+    b3g_status st = check_device(h->device);
+    if (st != B3G_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    RecordArgs ra = record_args(h->state, h->kw, kRecFinalize);
+    if (h->count <= kChunkBytes) {
+        ra.mode = kRecChunk;
+        ra.in = h->state + kBufOff;
+        ra.len = static_cast<uint32_t>(h->count);
+        ra.pushed = 0;
+    } else {
+        ra.depth = h->depth;
+        ra.pushed = h->pushed;
+        ra.len = h->buf_len;
+    }
+    st = launch_record(ra, s);
+    if (st != B3G_OK) return st;
+    return launch_xof(reinterpret_cast<const uint32_t *>(h->state + kRecordOff), d_out, out_len, s);
+}
+
+}  // extern "C"

@@ -79,8 +79,9 @@ int blake3_default_leaves_log2(void);
  * blake3_keyed_hash -- the digest of d_in[0..len) under `key`, written to d_out32.
  * Page sections "BLAKE3" (chunking, tree rules), "Kernel 1" (leaf kernel with the
  * fused subtree), "Kernel 2 和 3" (reduction of the subtree roots, ROOT last).
- * Temporary device memory (32 bytes per 256 chunks) comes from the stream-ordered
- * allocator (cudaMallocAsync/cudaFreeAsync on `stream`).
+ * Temporary device memory (32 bytes per CTA subtree: per 256 chunks, or per 32..128
+ * chunks for inputs of at most 64 MiB) comes from the stream-ordered allocator
+ * (cudaMallocAsync/cudaFreeAsync on `stream`).
  * Errors: B3G_ERR_NULL (key or d_out32 NULL, or d_in NULL with len > 0),
  * B3G_ERR_CUDA.
  */
@@ -179,6 +180,51 @@ b3g_status blake3_device_status(uint32_t *status_out);
  * word.  Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_CUDA.
  */
 b3g_status blake3_selftest_bounded_wait(uint32_t limit_us, int *timed_out_out);
+
+/*
+ * blake3_keyed_hash_xof -- out_len bytes of extendable output for d_in[0..len) under
+ * `key`, written to d_out (any alignment).  The first 32 bytes equal the digest of
+ * blake3_keyed_hash.  Output block i (bytes 64i .. 64i+63) is the root compression
+ * with ROOT set and its counter equal to i (BLAKE3 specification, extendable output;
+ * the page lists this mode under "未来工作" as not implemented).  Temporary device
+ * memory comes from the stream-ordered allocator.
+ * Errors: B3G_ERR_NULL, B3G_ERR_ARG (out_len beyond 2^31 * 16 KiB), B3G_ERR_CUDA.
+ */
+b3g_status blake3_keyed_hash_xof(const void *d_in, uint64_t len, const uint8_t key[32],
+                                 uint8_t *d_out, uint64_t out_len, b3g_stream_t stream);
+
+/*
+ * Streaming hasher: the digest of input that arrives as successive device segments of
+ * any length, equal to the digest of their concatenation.  The hasher is a host object
+ * that owns about 3 KiB of device memory on the device current at creation; every call
+ * must be made with that device current (else B3G_ERR_ARG).  Calls are asynchronous on
+ * the stream passed; a hasher must be used from one stream at a time (calls in stream
+ * order), and a segment may be reused once the update's work on that stream is done.
+ * Whole runs of chunks inside a segment go through the same leaf and reduction
+ * kernels as blake3_keyed_hash; chaining values are merged only once more input is
+ * known to follow (page section "BLAKE3": the tree rules).
+ */
+typedef struct b3g_hasher b3g_hasher;
+
+/* Creates a hasher for `key` (host pointer, copied).  Allocates with cudaMalloc. */
+b3g_status blake3_hasher_new(const uint8_t key[32], b3g_hasher **out);
+
+/* Frees the hasher and its device memory (cudaFree synchronises the device). */
+void blake3_hasher_free(b3g_hasher *h);
+
+/* Forgets all input (same key).  Host-side only. */
+b3g_status blake3_hasher_reset(b3g_hasher *h);
+
+/* Bytes absorbed so far. */
+uint64_t blake3_hasher_count(const b3g_hasher *h);
+
+/* Absorbs d_in[0..len).  Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_CUDA. */
+b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b3g_stream_t stream);
+
+/* Writes out_len bytes of output (32 for the digest) to d_out.  The hasher is not
+ * changed: more input may follow.  Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_CUDA. */
+b3g_status blake3_hasher_finalize(const b3g_hasher *h, uint8_t *d_out, uint64_t out_len,
+                                  b3g_stream_t stream);
 
 /*
  * blake3_keyed_hash_noalloc -- the same digest as blake3_keyed_hash, computed without

@@ -61,10 +61,11 @@ def _load():
         lib.oracle_subtree_cv.argtypes = [c_u8p, u64, u64, c_u8p, ctypes.c_int, c_u8p]
         lib.oracle_chunk_cvs.argtypes = [c_u8p, u64, u64, c_u8p, c_u8p]
         lib.oracle_blake2s_256.argtypes = [c_u8p, ctypes.c_size_t, c_u8p]
+        lib.oracle_keyed_hash_xof.argtypes = [c_u8p, u64, c_u8p, c_u8p, u64]
         for name in ("oracle_iv", "oracle_msg_permutation", "oracle_flags", "oracle_compress",
                      "oracle_chunk_cv", "oracle_parent_cv", "oracle_keyed_hash",
                      "oracle_keyed_hash_recursive", "oracle_subtree_cv", "oracle_chunk_cvs",
-                     "oracle_blake2s_256"):
+                     "oracle_blake2s_256", "oracle_keyed_hash_xof"):
             getattr(lib, name).restype = None
         _lib = lib
         return lib
@@ -172,6 +173,15 @@ def chunk_cvs(data, key, chunk_offset: int = 0) -> np.ndarray:
     _load().oracle_chunk_cvs(p, n, chunk_offset, _key(key), out.ctypes.data)
     del keep
     return out
+
+
+def keyed_hash_xof(data, key, out_len: int) -> bytes:
+    """out_len bytes of extendable output (root compression repeated with counter i)."""
+    p, n, keep = _buf(data)
+    out = ctypes.create_string_buffer(max(1, out_len))
+    _load().oracle_keyed_hash_xof(p, n, _key(key), out, out_len)
+    del keep
+    return out.raw[:out_len]
 
 
 def blake2s_256(data) -> bytes:

@@ -288,6 +288,82 @@ static void stack_merge_words(const uint32_t key[8], const uint8_t *buf, uint64_
 }
 
 /* ------------------------------------------------------------------------------ */
+/* Extendable output (BLAKE3 specification, section 2.6; the page lists it as      */
+/* future work).  The root compression is not evaluated once but kept as its       */
+/* inputs (CV, message block, block length, flags); output block i is that        */
+/* compression with ROOT and the counter set to i, all 16 output words.           */
+/* ------------------------------------------------------------------------------ */
+
+typedef struct {
+    uint32_t cv[8];
+    uint32_t block[16];
+    uint32_t block_len;
+    uint32_t flags; /* without ROOT */
+} root_inputs;
+
+static void root_of_chunk(const uint32_t key[8], const uint8_t *chunk, size_t chunk_len, root_inputs *out) {
+    size_t nblocks = chunk_len == 0 ? 1 : (chunk_len + BLOCK_LEN - 1) / BLOCK_LEN;
+    uint32_t cv[8];
+    memcpy(cv, key, sizeof cv);
+    for (size_t b = 0; b < nblocks; b++) {
+        uint8_t padded[BLOCK_LEN];
+        uint32_t m[16];
+        size_t start = b * BLOCK_LEN;
+        size_t take = chunk_len - start < BLOCK_LEN ? chunk_len - start : BLOCK_LEN;
+        memset(padded, 0, sizeof padded);
+        if (take) memcpy(padded, chunk + start, take);
+        words_from_bytes(padded, 16, m);
+        uint32_t flags = F_KEYED_HASH | (b == 0 ? F_CHUNK_START : 0u);
+        if (b + 1 == nblocks) {
+            memcpy(out->cv, cv, sizeof cv);
+            memcpy(out->block, m, sizeof m);
+            out->block_len = (uint32_t)take;
+            out->flags = flags | F_CHUNK_END;
+            return;
+        }
+        uint32_t o[16];
+        compress_words(cv, m, 0, (uint32_t)take, flags, o);
+        memcpy(cv, o, sizeof cv);
+    }
+}
+
+/* Root inputs of the whole input: the single chunk's last block, or the top
+ * parent whose children are the largest power-of-two left subtree and the rest. */
+static void root_inputs_of(const uint32_t key[8], const uint8_t *buf, uint64_t len, root_inputs *out) {
+    uint64_t n = num_chunks(len);
+    if (n == 1) {
+        root_of_chunk(key, buf, chunk_bytes(len, 0), out);
+        return;
+    }
+    uint64_t left_n = largest_pow2_below(n);
+    uint32_t l[8], r[8];
+    subtree_words(key, buf, len, 0, left_n, 0, 0, l);
+    subtree_words(key, buf, len, left_n, n - left_n, 0, 0, r);
+    memcpy(out->cv, key, 8 * sizeof(uint32_t));
+    memcpy(out->block, l, 8 * sizeof(uint32_t));
+    memcpy(out->block + 8, r, 8 * sizeof(uint32_t));
+    out->block_len = BLOCK_LEN;
+    out->flags = F_KEYED_HASH | F_PARENT;
+}
+
+/* out_len bytes of extendable output; the first 32 equal oracle_keyed_hash. */
+void oracle_keyed_hash_xof(const uint8_t *buf, uint64_t len, const uint8_t key[32], uint8_t *out,
+                           uint64_t out_len) {
+    uint32_t k[8];
+    words_from_bytes(key, 8, k);
+    root_inputs ri;
+    root_inputs_of(k, buf, len, &ri);
+    for (uint64_t i = 0; i * 64 < out_len; i++) {
+        uint32_t o[16];
+        uint8_t blk[64];
+        compress_words(ri.cv, ri.block, i, ri.block_len, ri.flags | F_ROOT, o);
+        bytes_from_words(o, 16, blk);
+        uint64_t take = out_len - i * 64 < 64 ? out_len - i * 64 : 64;
+        memcpy(out + i * 64, blk, (size_t)take);
+    }
+}
+
+/* ------------------------------------------------------------------------------ */
 /* BLAKE2s (RFC 7693) on the same round function: used only to pin G, its          */
 /* rotations, the column/diagonal assignment and IV against hashlib.blake2s.       */
 /* ------------------------------------------------------------------------------ */

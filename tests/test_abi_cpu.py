@@ -54,8 +54,14 @@ def test_sizes(lib):
     assert lib.blake3_tile_count(12 * (1 << 30) + 777, 8) == 49153
     assert lib.blake3_tile_count(1 << 20, 5) == 32
     assert lib.blake3_tile_count(1 << 20, 4) == 0
-    assert lib.blake3_workspace_size(256 * 1024) == 0  # one tile: no workspace
-    assert lib.blake3_workspace_size(1 << 20) == 4 * 32
+    assert lib.blake3_workspace_size(0) == 0  # one chunk, one tile: no workspace
+    assert lib.blake3_workspace_size(32 * 1024) == 0  # 32 chunks fit one 32-chunk tile
+    # small inputs spread over 32-chunk tiles: 1 MiB = 1024 chunks = 32 tiles
+    assert lib.blake3_workspace_size(1 << 20) == 32 * 32
+    assert lib.blake3_workspace_size(256 * 1024) == 8 * 32
+    # 64 MiB = 65536 chunks: 256-chunk tiles already give 256 CTAs
+    assert lib.blake3_workspace_size(64 << 20) == 256 * 32
+    assert lib.blake3_workspace_size(40 << 20) == 160 * 32  # 40960 chunks / 256
     # 4 GiB: 16384 tile CVs, then 16 group CVs
     assert lib.blake3_workspace_size(1 << 32) == 16384 * 32 + 16 * 32
     assert lib.blake3_reduce_workspace_size(1024, 10) == 0
@@ -100,3 +106,16 @@ def test_output_alignment_is_checked(lib):
     assert lib.blake3_keyed_subtree_root(FAKE, 10, 0, KEY, 1, odd, None) == 2
     assert lib.blake3_keyed_tile_roots(FAKE, 10, 0, KEY, -1, 1, odd, None) == 2
     assert lib.blake3_keyed_reduce_cvs(odd, 4, KEY, 1, -1, FAKE, FAKE, 0, None) == 2
+
+
+def test_stream_and_xof_argument_errors(lib):
+    h = ctypes.c_void_p()
+    assert lib.blake3_hasher_new(None, ctypes.byref(h)) == 1
+    assert lib.blake3_hasher_new(KEY, None) == 1
+    assert lib.blake3_hasher_update(None, FAKE, 10, None) == 1
+    assert lib.blake3_hasher_finalize(None, FAKE, 32, None) == 1
+    assert lib.blake3_hasher_reset(None) == 1
+    assert lib.blake3_hasher_count(None) == 0
+    lib.blake3_hasher_free(None)
+    assert lib.blake3_keyed_hash_xof(FAKE, 10, None, FAKE, 32, None) == 1
+    assert lib.blake3_keyed_hash_xof(FAKE, 10, KEY, None, 32, None) == 1

@@ -1,0 +1,107 @@
+"""GPU parity of the extendable output and of the streaming hasher against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from blake3_merkle_tree_gb300 import binding, workloads
+
+pytestmark = pytest.mark.gpu
+
+KEY = workloads.key_bytes(11)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from blake3_merkle_tree_gb300 import build
+
+    build.build()
+    binding.library()
+    yield
+    assert binding.blake3_device_status() == 0
+
+
+@pytest.mark.parametrize("length", [0, 1, 64, 1024, 1025, 2048, 13 * 1024 + 7, 300 * 1024 + 3, 3 * (1 << 20) + 5])
+@pytest.mark.parametrize("out_len", [0, 1, 31, 32, 33, 64, 65, 1000, 4096 + 7])
+def test_xof(length, out_len):
+    host = workloads.uniform_bytes(length + 3, length)
+    got = binding.blake3_keyed_hash_xof(host.cuda(), KEY, out_len)
+    ref = oracle.keyed_hash_xof(host, KEY, out_len)
+    assert bytes(got.cpu().numpy()) == ref
+
+
+def test_xof_misaligned_output_and_long_output():
+    host = workloads.uniform_bytes(5, (1 << 20) + 17)
+    d = host.cuda()
+    buf = torch.zeros((8 << 20) + 64, dtype=torch.uint8, device="cuda")
+    out = buf[3:3 + (8 << 20) + 5]
+    binding.blake3_keyed_hash_xof(d, KEY, out.numel(), out=out)
+    ref = oracle.keyed_hash_xof(host, KEY, out.numel())
+    assert bytes(out.cpu().numpy()) == ref
+    assert int(buf[:3].sum()) == 0 and int(buf[3 + out.numel():].sum()) == 0  # nothing written outside
+    assert bytes(out[:32].cpu().numpy()) == bytes(binding.blake3_keyed_hash(d, KEY).cpu().numpy())
+
+
+def _splits(total, parts, seed):
+    rng = np.random.default_rng(seed)
+    cuts = sorted(int(x) for x in rng.integers(0, total + 1, parts - 1)) if total and parts > 1 else []
+    pts = [0] + cuts + [total]
+    return [(pts[i], pts[i + 1]) for i in range(len(pts) - 1)]
+
+
+@pytest.mark.parametrize("total", [0, 1, 1023, 1024, 1025, 2048, 2049, 5000, 64 * 1024, 300 * 1024 + 3,
+                                   (4 << 20) + 777])
+@pytest.mark.parametrize("parts", [1, 2, 3, 7, 20])
+def test_hasher_random_segments(total, parts):
+    host = workloads.uniform_bytes(total + 101, total)
+    d = host.cuda()
+    h = binding.Hasher(KEY)
+    for a, b in _splits(total, parts, seed=total * 31 + parts):
+        h.update(d[a:b])
+    assert h.count == total
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
+    assert bytes(h.finalize(200).cpu().numpy()) == oracle.keyed_hash_xof(host, KEY, 200)
+    h.close()
+
+
+@pytest.mark.parametrize("seg", [1024, 4096, 256 * 1024, 1 << 20])
+def test_hasher_chunk_aligned_segments(seg):
+    total = 6 * seg + 1024 * 3
+    host = workloads.uniform_bytes(seg, total)
+    d = host.cuda()
+    h = binding.Hasher(KEY)
+    for a in range(0, total, seg):
+        h.update(d[a:a + seg])
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
+
+
+def test_hasher_finalize_then_continue_and_reset():
+    total = 3 * (1 << 20) + 99
+    host = workloads.uniform_bytes(77, total)
+    d = host.cuda()
+    h = binding.Hasher(KEY)
+    for cut in (1000, 5000, 70 * 1024, 1 << 20):
+        h.update(d[h.count:cut])
+        assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host[:cut], KEY), cut
+    h.update(d[h.count:])
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
+    h.reset()
+    assert h.count == 0
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(b"", KEY)
+    h.update(d[:5000])
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host[:5000], KEY)
+
+
+def test_hasher_large_matches_one_shot():
+    """64 MiB segments with a ragged end: equal to the one-shot GPU digest and the oracle."""
+    w = workloads.WORKLOADS["bf16_256MiB"]
+    host = w.data()
+    d = host.cuda()
+    h = binding.Hasher(w.key())
+    seg = 64 << 20
+    for a in range(0, d.numel(), seg - 777):
+        h.update(d[a:a + seg - 777])
+    got = bytes(h.finalize().cpu().numpy())
+    assert got == bytes(binding.blake3_keyed_hash(d, w.key()).cpu().numpy())
+    assert got == oracle.keyed_hash(host, w.key())

@@ -201,3 +201,31 @@ def test_counter_is_per_chunk():
     assert len({a, b, c}) == 3
     cvs = oracle.chunk_cvs(np.frombuffer(block * 3, dtype=np.uint8), KEY)
     assert bytes(cvs[0]) == a and bytes(cvs[1]) == b
+
+
+@pytest.mark.parametrize("length", [0, 1, 64, 1024, 1025, 13 * 1024 + 7, 100 * 1024])
+def test_xof_prefix_is_the_digest(length):
+    """Extendable output: its first 32 bytes are the digest (the digest is output block 0
+    truncated), and a shorter output is a prefix of a longer one."""
+    data = _data(length, seed=500 + length)
+    digest = oracle.keyed_hash(data, KEY)
+    long = oracle.keyed_hash_xof(data, KEY, 1000)
+    assert long[:32] == digest
+    assert oracle.keyed_hash_xof(data, KEY, 32) == digest
+    for n in (0, 1, 63, 64, 65, 200):
+        assert oracle.keyed_hash_xof(data, KEY, n) == long[:n]
+    # output blocks differ from one another (the counter advances)
+    blocks = [long[i:i + 64] for i in range(0, 960, 64)]
+    assert len(set(blocks)) == len(blocks)
+
+
+def test_xof_block_is_the_root_compression_with_counter():
+    """Two-chunk input: output block i == compress(key, left||right, i, 64, KEYED|PARENT|ROOT)."""
+    f = oracle.flags()
+    data = _data(2048, seed=8)
+    left = oracle.chunk_cv(KEY, data[:1024], 0)
+    right = oracle.chunk_cv(KEY, data[1024:], 1)
+    out = oracle.keyed_hash_xof(data, KEY, 64 * 5)
+    for i in range(5):
+        blk = oracle.compress(KEY, left + right, i, 64, f["KEYED_HASH"] | f["PARENT"] | f["ROOT"])
+        assert out[64 * i:64 * (i + 1)] == blk
