@@ -311,31 +311,32 @@ def run_ours(args):
 
 
 def _e2e(args, binding, dev, key, out, stream, digest_api, world):
+    """The digest of the workload from pinned host memory through blake3_keyed_hash_host:
+    every step copies the whole input host->device (overlapped with hashing inside the
+    call) and returns the 32-byte digest to the host."""
     n = dev.numel()
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     host = torch.empty(n, dtype=torch.uint8, pin_memory=True)
     host.copy_(dev)
-    host_out = torch.empty(32, dtype=torch.uint8, pin_memory=True)
+    staging = torch.empty(3328 + 2 * (256 << 20), dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
-    for _ in range(1):
-        dev.copy_(host, non_blocking=True)
-        binding.blake3_keyed_hash(dev, key, out=out)
-        host_out.copy_(out, non_blocking=True)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    got = binding.blake3_keyed_hash_host(host, key, staging)  # warm-up
+    t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        dev.copy_(host, non_blocking=True)
-        binding.blake3_keyed_hash(dev, key, out=out)
-        host_out.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if bytes(host_out.numpy()) != digest_api:
+        got = binding.blake3_keyed_hash_host(host, key, staging)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if got != digest_api:
         raise RuntimeError("end-to-end digest differs")
-    e2e = {"value": world * n / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": n,
-           "d2h_bytes_per_step": 32, "ms_per_step": e2e_ms, "steps": e2e_steps}
+    # context: one plain host->device copy of the same pinned buffer
+    torch.cuda.synchronize()
+    c0 = time.perf_counter()
+    dev.copy_(host, non_blocking=True)
+    torch.cuda.synchronize()
+    h2d_gbs = n / (time.perf_counter() - c0) / 1e9
+    e2e = {"value": world * n / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": n,
+           "d2h_bytes_per_step": 32, "ms_per_step": e2e_s * 1e3, "steps": e2e_steps,
+           "call": "blake3_keyed_hash_host (pinned host input, 2 x 256 MiB device staging)",
+           "plain_h2d_copy_GBps": h2d_gbs}
     return e2e, host
 
 

@@ -17,6 +17,7 @@ _BINDING_NAMES = (
     "blake3_keyed_hash_ws",
     "blake3_keyed_hash_noalloc",
     "blake3_keyed_hash_xof",
+    "blake3_keyed_hash_host",
     "Hasher",
     "blake3_workspace_size",
     "blake3_keyed_chunk_cvs",

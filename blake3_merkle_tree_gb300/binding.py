@@ -68,6 +68,7 @@ def library() -> ctypes.CDLL:
             "blake3_hasher_count": (u64, [vp]),
             "blake3_hasher_update": (i32, [vp, vp, u64, vp]),
             "blake3_hasher_finalize": (i32, [vp, vp, u64, vp]),
+            "blake3_keyed_hash_host": (i32, [vp, u64, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -285,3 +286,18 @@ class Hasher:
             self.close()
         except Exception:
             pass
+
+
+def blake3_keyed_hash_host(data: torch.Tensor, key, staging: torch.Tensor | None = None, stream=None) -> bytes:
+    """Digest of a contiguous HOST tensor (pinned for full speed), copied and hashed in
+    overlapping segments; returns the 32 digest bytes."""
+    if data.is_cuda:
+        raise ValueError("data must be a host tensor")
+    t = data.contiguous()
+    out = ctypes.create_string_buffer(32)
+    st_ptr = _dev_ptr(staging, "staging") if staging is not None else None
+    st_bytes = _nbytes(staging) if staging is not None else 0
+    st = library().blake3_keyed_hash_host(t.data_ptr() if t.numel() else None, _nbytes(t), _key(key), out,
+                                          st_ptr, st_bytes, _stream(stream))
+    _check(st, "blake3_keyed_hash_host")
+    return out.raw

@@ -14,7 +14,7 @@ namespace b3g {
 constexpr uint64_t kChunkBytes = 1024;
 constexpr int kMinLeavesLog2 = 5;
 constexpr int kMaxLeavesLog2 = 8;
-constexpr int kDefaultLeavesLog2 = 8;
+constexpr int kDefaultLeavesLog2 = 7;  // 128 chunks per CTA (measured best on GB300)
 constexpr int kMaxGroupLog2 = 10;
 constexpr int kDefaultGroupLog2 = 10;
 // Default limit of every device-side wait: far above any real wait (microseconds),

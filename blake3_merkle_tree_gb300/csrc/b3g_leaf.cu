@@ -44,68 +44,68 @@ namespace b3g {
 constexpr uint32_t kBarTree = 1;  // named barrier id of the consumer threads
 
 // ---------------------------------------------------------------------------------
-// Bulk-tensor-copy (TMA) pipeline kernel, warp specialised:
-//   warps 0 .. C/32-1   consumers: one chunk per thread, 16 chained compressions
-//   warp  C/32          producer: one lane issues the bulk tensor copies
-//   warp  C/32+1        reducer: reduces each tile's C chunk CVs to the tile CV
+// Bulk-tensor-copy (TMA) kernel.
+//   warps 0 .. C/32-1   consumers: thread r compresses chunk tile*C + r (16 chained
+//                       compressions).  Each consumer warp feeds itself: its lane 0
+//                       keeps S bulk tensor copies of the warp's own 32 chunk rows
+//                       (LOAD bytes of each row per copy) in flight in a private ring
+//                       of S stages, and refills a stage right after the warp has
+//                       consumed it.  No warp waits for another warp's progress.
+//   warp  C/32          reducer: reduces each tile's C chunk CVs to the tile CV.
 // The consumers hand their chunk CVs to the reducer through two node buffers
 // (tile k uses buffer k&1) guarded by mbarriers, so a consumer never waits for the
 // tree of the previous tile: it stores its CV, arrives, and starts the next tile.
 //
 //   C          consumers = chunks per tile (2^t), a multiple of 32, at most 256
-//   S          stages in the shared-memory ring
-//   LOAD       bytes of every chunk brought by one load (128 or 64)
+//   S          stages in each consumer warp's ring
+//   LOAD       bytes of every chunk brought by one copy (128 or 64)
 //   CHUNK_CVS  write every chunk CV instead of reducing the tile (no reducer work)
 // ---------------------------------------------------------------------------------
 template <int C, int S, int LOAD, bool CHUNK_CVS>
 struct TmaCfg {
     static_assert(C % 32 == 0 && C >= 32 && C <= 256, "consumer count");
     static_assert(LOAD == 128 || LOAD == 64, "load width");
-    static constexpr int kLoadsPerTile = 1024 / LOAD;
+    static constexpr int kLoadsPerChunk = 1024 / LOAD;
     static constexpr int kBlocksPerLoad = LOAD / 64;
-    static constexpr uint32_t kStageBytes = C * LOAD;
     static constexpr int kConsumerWarps = C / 32;
-    static constexpr int kProducerWarp = kConsumerWarps;
-    static constexpr int kReducerWarp = kConsumerWarps + 1;
-    static constexpr int kThreads = C + 64;
-    static constexpr uint32_t kNodeBytes = C * 32;                  // one node buffer
-    static constexpr uint32_t kScratch1Bytes = (C / 2) * 32;        // odd tree levels
-    static constexpr uint32_t kScratch2Bytes = (C / 4 < 1 ? 1 : C / 4) * 32;  // even levels
-    // layout: [align 1024][S stages][2 node buffers][scratch 1][scratch 2][barriers]
-    static constexpr uint32_t kOffNodes = S * kStageBytes;
+    static constexpr int kReducerWarp = kConsumerWarps;
+    static constexpr int kThreads = C + 32;
+    static constexpr uint32_t kRowsPerCopy = 32;                    // one warp's rows
+    static constexpr uint32_t kStageBytes = kRowsPerCopy * LOAD;  // = the copy's box bytes
+    static constexpr uint32_t kRingBytes = S * kStageBytes;
+    static constexpr uint32_t kNodeBytes = C * 32;            // one node buffer
+    static constexpr uint32_t kScratch1Bytes = (C / 2) * 32;  // odd tree levels
+    static constexpr uint32_t kScratch2Bytes = (C / 4) * 32;  // even tree levels
+    // layout: [align 1024][rings][2 node buffers][scratch 1][scratch 2][barriers]
+    static constexpr uint32_t kOffNodes = kConsumerWarps * kRingBytes;
     static constexpr uint32_t kOffScratch1 = kOffNodes + 2 * kNodeBytes;
     static constexpr uint32_t kOffScratch2 = kOffScratch1 + kScratch1Bytes;
     static constexpr uint32_t kOffBars = kOffScratch2 + kScratch2Bytes;
-    static constexpr uint32_t kNumBars = 2 * S + 4;
+    static constexpr uint32_t kNumBars = kConsumerWarps * S + 4;
     static constexpr size_t kSmemBytes = 1024 + size_t(kOffBars) + 8 * kNumBars;
-    static_assert(S >= 2, "stage count");
+    static_assert(S >= 2 && S <= kLoadsPerChunk, "stage count");
 };
 
 template <int C, int S, int LOAD, bool CHUNK_CVS>
-__global__ void __launch_bounds__(C + 64)
+__global__ void __launch_bounds__(C + 32)
     leaf_tma_kernel(const __grid_constant__ CUtensorMap tmap, const LeafArgs a) {
     using Cfg = TmaCfg<C, S, LOAD, CHUNK_CVS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t stage0 = (raw + 1023u) & ~1023u;
-    const uint32_t nodes0 = stage0 + Cfg::kOffNodes;  // buffer b at nodes0 + b * kNodeBytes
-    const uint32_t scratch1 = stage0 + Cfg::kOffScratch1;
-    const uint32_t scratch2 = stage0 + Cfg::kOffScratch2;
-    const uint32_t full0 = stage0 + Cfg::kOffBars;  // S barriers, 8 bytes each
-    const uint32_t empty0 = full0 + 8 * S;          // S barriers
-    const uint32_t cvfull0 = empty0 + 8 * S;        // 2 barriers: node buffer b is filled
-    const uint32_t cvempty0 = cvfull0 + 16;         // 2 barriers: node buffer b is free
+    const uint32_t rings0 = (raw + 1023u) & ~1023u;
+    const uint32_t nodes0 = rings0 + Cfg::kOffNodes;  // buffer b at nodes0 + b * kNodeBytes
+    const uint32_t scratch1 = rings0 + Cfg::kOffScratch1;
+    const uint32_t scratch2 = rings0 + Cfg::kOffScratch2;
+    const uint32_t full0 = rings0 + Cfg::kOffBars;               // S barriers per consumer warp
+    const uint32_t cvfull0 = full0 + 8 * Cfg::kConsumerWarps * S;  // 2: node buffer b is filled
+    const uint32_t cvempty0 = cvfull0 + 16;                        // 2: node buffer b is free
 
     const uint32_t tid = threadIdx.x;
     const uint32_t warp = tid >> 5;
     const uint32_t lane = tid & 31u;
 
     if (tid == 0) {
-#pragma unroll
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, Cfg::kConsumerWarps);
-        }
+        for (int i = 0; i < Cfg::kConsumerWarps * S; ++i) mbar_init(full0 + 8 * i, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(cvfull0 + 8 * b, C);
             mbar_init(cvempty0 + 8 * b, 32);
@@ -113,38 +113,6 @@ __global__ void __launch_bounds__(C + 64)
         fence_mbar_init();
     }
     __syncthreads();
-
-    if (warp == Cfg::kProducerWarp) {
-        // ------------------------------- producer -------------------------------
-        if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap) : "memory");
-            uint32_t it = 0;
-            bool ok = true;
-            for (uint64_t tile = blockIdx.x; ok && tile < a.n_tiles; tile += gridDim.x) {
-                for (int ld = 0; ld < Cfg::kLoadsPerTile; ++ld, ++it) {
-                    const uint32_t s = it % S;
-                    const uint32_t k = it / S;
-                    if (k > 0 && !mbar_wait_bounded(empty0 + 8 * s, (k - 1) & 1u, a.wait_limit_ns)) {
-                        atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(full0 + 8 * s, Cfg::kStageBytes);
-                    tma_load_2d(stage0 + s * Cfg::kStageBytes, &tmap, ld * (LOAD / 4),
-                                static_cast<int32_t>(tile * C), full0 + 8 * s);
-                }
-            }
-            // Drain: wait (bounded) for the last loads issued, so that no copy into
-            // this CTA's shared memory is still in flight when it exits.  On the
-            // normal path the consumers have already waited for them.
-            const uint32_t inflight = it < S ? it : S;
-            for (uint32_t j = 0; j < inflight; ++j) {
-                const uint32_t u = it - 1 - j;
-                mbar_wait_bounded(full0 + 8 * (u % S), (u / S) & 1u, a.wait_limit_ns);
-            }
-        }
-        return;
-    }
 
     uint32_t key[8];
 #pragma unroll
@@ -206,11 +174,36 @@ __global__ void __launch_bounds__(C + 64)
 
     // --------------------------------- consumers ---------------------------------
     const uint32_t r = tid;
-    // 16-byte unit u of this thread's row sits at u ^ swz (TMA 128B / 64B swizzle)
-    const uint32_t swz = LOAD == 128 ? (r & 7u) : ((r >> 1) & 3u);
-    const uint32_t row_off = r * LOAD;
-    uint32_t it = 0;
+    const uint32_t ring = rings0 + warp * Cfg::kRingBytes;
+    const uint32_t fullw = full0 + 8 * S * warp;
+    // 16-byte unit u of row `lane` sits at u ^ swz (TMA 128B / 64B swizzle)
+    const uint32_t swz = LOAD == 128 ? (lane & 7u) : ((lane >> 1) & 3u);
+    const uint32_t row_off = lane * LOAD;
+
+    // Copy stream of this warp: copy i brings part (i mod kLoadsPerChunk) of the warp's
+    // rows of tile blockIdx.x + (i / kLoadsPerChunk) * gridDim.x.  Only lane 0 issues.
+    uint64_t next_tile = blockIdx.x;
+    uint32_t next_part = 0;
+    uint32_t issued = 0, consumed = 0;
+    auto issue = [&](uint32_t stage) {
+        if (next_tile >= a.n_tiles) return;
+        mbar_arrive_expect_tx(fullw + 8 * stage, Cfg::kStageBytes);
+        tma_load_2d(ring + stage * Cfg::kStageBytes, &tmap, static_cast<int32_t>(next_part * (LOAD / 4)),
+                    static_cast<int32_t>(next_tile * C + Cfg::kRowsPerCopy * warp), fullw + 8 * stage);
+        ++issued;
+        if (++next_part == Cfg::kLoadsPerChunk) {
+            next_part = 0;
+            next_tile += gridDim.x;
+        }
+    };
+    if (lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap) : "memory");
+        for (int i = 0; i < S; ++i) issue(static_cast<uint32_t>(i));
+    }
+
+    uint32_t s = 0, ph = 0;  // stage of the next copy to consume and its fill parity
     uint32_t k = 0;
+    bool aborted = false;
 
     for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
         const uint64_t chunk = tile * C + r;
@@ -227,17 +220,14 @@ __global__ void __launch_bounds__(C + 64)
 #pragma unroll
         for (int i = 0; i < 8; ++i) cv[i] = key[i];
 
-        bool aborted = false;
 #pragma unroll 1
-        for (int ld = 0; ld < Cfg::kLoadsPerTile; ++ld, ++it) {
-            const uint32_t s = it % S;
-            const uint32_t kk = it / S;
-            if (!mbar_wait_bounded(full0 + 8 * s, kk & 1u, a.wait_limit_ns)) {
+        for (int ld = 0; ld < Cfg::kLoadsPerChunk; ++ld) {
+            if (!mbar_wait_bounded(fullw + 8 * s, ph, a.wait_limit_ns)) {
                 atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
                 aborted = true;
                 break;
             }
-            const uint32_t rowp = stage0 + s * Cfg::kStageBytes + row_off;
+            const uint32_t rowp = ring + s * Cfg::kStageBytes + row_off;
 #pragma unroll
             for (int j = 0; j < Cfg::kBlocksPerLoad; ++j) {
                 const uint32_t b = ld * Cfg::kBlocksPerLoad + j;
@@ -259,8 +249,18 @@ __global__ void __launch_bounds__(C + 64)
                 const uint32_t flags = kKeyedHash | (b == 0 ? kChunkStart : 0u) | (last ? end_flags : 0u);
                 if (b < nblocks) compress(cv, m, ctr_lo, ctr_hi, last ? last_len : 64u, flags);
             }
+            // every lane has consumed stage s (its words went into the compression):
+            // refill it with the copy S positions ahead
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            ++consumed;
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s);
+            }
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
         if (aborted) break;
 
@@ -276,10 +276,20 @@ __global__ void __launch_bounds__(C + 64)
             const uint32_t b = k & 1u;
             if (k >= 2 && !mbar_wait_bounded(cvempty0 + 8 * b, ((k >> 1) - 1) & 1u, a.wait_limit_ns)) {
                 atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
+                aborted = true;
                 break;
             }
             if (valid) store_node(nodes0 + b * Cfg::kNodeBytes, r, cv);
             mbar_arrive(cvfull0 + 8 * b);
+        }
+    }
+    // After a give-up, wait (bounded) for this warp's copies still in flight, so that
+    // none lands in shared memory after the CTA has left.  Without a give-up every
+    // copy issued has been consumed.
+    if (aborted && lane == 0) {
+        for (uint32_t i = consumed; i < issued; ++i) {
+            const uint32_t st = i % S;
+            mbar_wait_bounded(fullw + 8 * st, (i / S) & 1u, a.wait_limit_ns);
         }
     }
 }
@@ -360,7 +370,7 @@ constexpr int kMaxDevices = 64;
 #define B3G_TUNE_LOAD256 64
 #endif
 #ifndef B3G_TUNE_S128
-#define B3G_TUNE_S128 4
+#define B3G_TUNE_S128 3
 #endif
 #ifndef B3G_TUNE_LOAD128
 #define B3G_TUNE_LOAD128 64
@@ -463,7 +473,9 @@ b3g_status launch_tma(const LeafArgs &a, cudaStream_t stream, int dev, const Dev
     CUtensorMap tmap;
     cuuint64_t gdim[2] = {256, static_cast<cuuint64_t>(a.n_full)};
     cuuint64_t gstride[1] = {1024};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(T::LOAD / 4), static_cast<cuuint32_t>(C)};
+    // box = one warp's rows, LOAD bytes of each: exactly one stage (kStageBytes)
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(T::LOAD / 4), Cfg::kRowsPerCopy};
+    static_assert(Cfg::kStageBytes == Cfg::kRowsPerCopy * T::LOAD, "box and stage size must agree");
     cuuint32_t estride[2] = {1, 1};
     CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t *>(a.in), gdim, gstride,
                          box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,

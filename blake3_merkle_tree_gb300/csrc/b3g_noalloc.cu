@@ -27,6 +27,8 @@ namespace {
 // 65,536 CTA roots (16 GiB of input at 256 chunks per CTA) plus the 64 CVs of the
 // next reduction level, rounded up.
 constexpr size_t kNoAllocScratchBytes = (2u << 20) + 4096;
+// 256 chunks per CTA subtree: the scratch size above is computed for it.
+constexpr int kNoAllocLeavesLog2 = 8;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -68,7 +70,7 @@ extern "C" b3g_status blake3_keyed_hash_noalloc(const void *d_in, uint64_t len, 
     if (len > B3G_NOALLOC_MAX_LEN) return B3G_ERR_WORKSPACE;
 
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int t = kDefaultLeavesLog2;
+    const int t = kNoAllocLeavesLog2;
     const uint64_t n_chunks = len == 0 ? 1 : ceil_div(len, kChunkBytes);
     const uint64_t tiles = ceil_div(n_chunks, 1ull << t);
     const uint64_t group = 1ull << kDefaultGroupLog2;

@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -254,6 +255,24 @@ b3g_status check_device(int want) {
     return dev == want ? B3G_OK : B3G_ERR_ARG;
 }
 
+// One non-blocking copy stream per device for blake3_keyed_hash_host, created on
+// first use and kept for the life of the process.
+b3g_status copy_stream(cudaStream_t *out) {
+    static std::mutex mu;
+    static cudaStream_t cache[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return B3G_ERR_ARG;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        e = cudaStreamCreateWithFlags(&cache[dev], cudaStreamNonBlocking);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
+    }
+    *out = cache[dev];
+    return B3G_OK;
+}
+
 }  // namespace
 }  // namespace b3g
 
@@ -465,6 +484,75 @@ b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b
     h->buf_len = static_cast<uint32_t>(tail);
     h->count += rest;
     return B3G_OK;
+}
+
+b3g_status blake3_keyed_hash_host(const void *h_in, uint64_t len, const uint8_t key[32], uint8_t out32[32],
+                                  void *d_staging, size_t staging_bytes, b3g_stream_t stream) {
+    if (!key || !out32 || (!h_in && len > 0)) return B3G_ERR_NULL;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t cs = nullptr;
+    b3g_status st = copy_stream(&cs);
+    if (st != B3G_OK) return st;
+    constexpr size_t kSlotAlign = 1u << 20;
+    constexpr size_t kHead = (kStateBytes + 255) & ~size_t(255);  // hasher state + digest
+    bool own = false;
+    if (!d_staging) {
+        staging_bytes = kHead + 2 * (64u << 20);
+        cudaError_t e = cudaMallocAsync(&d_staging, staging_bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
+        own = true;
+    }
+    if (reinterpret_cast<uintptr_t>(d_staging) & 255u) return B3G_ERR_ALIGN;
+    if (staging_bytes < kHead + 2 * kSlotAlign) return B3G_ERR_WORKSPACE;
+    const size_t slot = ((staging_bytes - kHead) / 2) & ~(kSlotAlign - 1);
+    uint8_t *base = static_cast<uint8_t *>(d_staging);
+    uint8_t *slots[2] = {base + kHead, base + kHead + slot};
+
+    b3g_hasher h;
+    std::memcpy(h.key, key, 32);
+    key_words(key, h.kw);
+    h.state = base;
+    h.count = h.pushed = 0;
+    h.depth = h.buf_len = 0;
+    cudaError_t e = cudaGetDevice(&h.device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+
+    cudaEvent_t ev[5] = {};
+    for (int i = 0; i < 5 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    cudaEvent_t start = ev[0], copied[2] = {ev[1], ev[2]}, consumed[2] = {ev[3], ev[4]};
+    if (e == cudaSuccess) e = cudaEventRecord(start, s);  // staging is free once the stream reaches here
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, start, 0);
+    if (e != cudaSuccess) st = cuda_fail(e, "event set-up");
+    const uint8_t *src = static_cast<const uint8_t *>(h_in);
+    uint64_t off = 0;
+    for (uint64_t i = 0; st == B3G_OK && off < len; ++i) {
+        const int b = static_cast<int>(i & 1);
+        const uint64_t n = len - off < slot ? len - off : slot;
+        if (i >= 2) e = cudaStreamWaitEvent(cs, consumed[b], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(slots[b], src + off, n, cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(copied[b], cs);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, copied[b], 0);
+        if (e != cudaSuccess) {
+            st = cuda_fail(e, "staging copy");
+            break;
+        }
+        st = blake3_hasher_update(&h, slots[b], n, stream);
+        if (st == B3G_OK && (e = cudaEventRecord(consumed[b], s)) != cudaSuccess) st = cuda_fail(e, "cudaEventRecord");
+        off += n;
+    }
+    uint8_t *d_digest = base + kStateBytes;  // 32 bytes between the state and the slots
+    if (st == B3G_OK) st = blake3_hasher_finalize(&h, d_digest, 32, stream);
+    if (st == B3G_OK && (e = cudaMemcpyAsync(out32, d_digest, 32, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        st = cuda_fail(e, "cudaMemcpyAsync(digest)");
+    if (own) {
+        e = cudaFreeAsync(d_staging, s);
+        if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
+    }
+    e = cudaStreamSynchronize(s);
+    if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaStreamSynchronize");
+    for (cudaEvent_t x : ev)
+        if (x) cudaEventDestroy(x);
+    return st;
 }
 
 b3g_status blake3_hasher_finalize(const b3g_hasher *h, uint8_t *d_out, uint64_t out_len, b3g_stream_t stream) {

@@ -72,14 +72,14 @@ const char *blake3_strerror(b3g_status status);
 /* Text of the last CUDA error seen by this thread inside the library ("" if none). */
 const char *blake3_last_cuda_error(void);
 
-/* Chunks per CTA subtree used when leaves_log2 is -1 (a power of two: 2^8 = 256). */
+/* Chunks per CTA subtree used when leaves_log2 is -1 (a power of two: 2^7 = 128). */
 int blake3_default_leaves_log2(void);
 
 /*
  * blake3_keyed_hash -- the digest of d_in[0..len) under `key`, written to d_out32.
  * Page sections "BLAKE3" (chunking, tree rules), "Kernel 1" (leaf kernel with the
  * fused subtree), "Kernel 2 和 3" (reduction of the subtree roots, ROOT last).
- * Temporary device memory (32 bytes per CTA subtree: per 256 chunks, or per 32..128
+ * Temporary device memory (32 bytes per CTA subtree: per 128 chunks, or per 32..64
  * chunks for inputs of at most 64 MiB) comes from the stream-ordered allocator
  * (cudaMallocAsync/cudaFreeAsync on `stream`).
  * Errors: B3G_ERR_NULL (key or d_out32 NULL, or d_in NULL with len > 0),
@@ -224,6 +224,22 @@ b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b
 /* Writes out_len bytes of output (32 for the digest) to d_out.  The hasher is not
  * changed: more input may follow.  Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_CUDA. */
 b3g_status blake3_hasher_finalize(const b3g_hasher *h, uint8_t *d_out, uint64_t out_len,
+                                  b3g_stream_t stream);
+
+/*
+ * blake3_keyed_hash_host -- the digest of HOST memory h_in[0..len), written to the host
+ * buffer out32.  The input is copied to the device in segments on an internal copy
+ * stream, into two alternating slots of the device buffer d_staging, while the other
+ * slot is hashed on `stream` by the streaming hasher (copies and hashing overlap).
+ * For full speed h_in should be page-locked (cudaHostAlloc / cudaHostRegister).
+ * d_staging (256-byte aligned, at least 3328 + 2 MiB bytes; its size sets the segment
+ * size) may be NULL: then 128 MiB + 3328 bytes come from the stream-ordered allocator.
+ * Synchronous: returns once the digest is in out32.
+ * Errors: B3G_ERR_NULL, B3G_ERR_ALIGN, B3G_ERR_WORKSPACE (d_staging too small),
+ * B3G_ERR_CUDA.
+ */
+b3g_status blake3_keyed_hash_host(const void *h_in, uint64_t len, const uint8_t key[32],
+                                  uint8_t out32[32], void *d_staging, size_t staging_bytes,
                                   b3g_stream_t stream);
 
 /*

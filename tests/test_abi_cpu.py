@@ -47,11 +47,12 @@ def test_strerror(lib):
 
 
 def test_sizes(lib):
-    assert lib.blake3_default_leaves_log2() == 8
+    assert lib.blake3_default_leaves_log2() == 7
     assert lib.blake3_tile_count(0, -1) == 1
-    assert lib.blake3_tile_count(256 * 1024, -1) == 1
-    assert lib.blake3_tile_count(256 * 1024 + 1, -1) == 2
+    assert lib.blake3_tile_count(128 * 1024, -1) == 1
+    assert lib.blake3_tile_count(128 * 1024 + 1, -1) == 2
     assert lib.blake3_tile_count(12 * (1 << 30) + 777, 8) == 49153
+    assert lib.blake3_tile_count(12 * (1 << 30) + 777, -1) == 98305
     assert lib.blake3_tile_count(1 << 20, 5) == 32
     assert lib.blake3_tile_count(1 << 20, 4) == 0
     assert lib.blake3_workspace_size(0) == 0  # one chunk, one tile: no workspace
@@ -59,11 +60,12 @@ def test_sizes(lib):
     # small inputs spread over 32-chunk tiles: 1 MiB = 1024 chunks = 32 tiles
     assert lib.blake3_workspace_size(1 << 20) == 32 * 32
     assert lib.blake3_workspace_size(256 * 1024) == 8 * 32
-    # 64 MiB = 65536 chunks: 256-chunk tiles already give 256 CTAs
-    assert lib.blake3_workspace_size(64 << 20) == 256 * 32
-    assert lib.blake3_workspace_size(40 << 20) == 160 * 32  # 40960 chunks / 256
-    # 4 GiB: 16384 tile CVs, then 16 group CVs
-    assert lib.blake3_workspace_size(1 << 32) == 16384 * 32 + 16 * 32
+    # 64 MiB = 65536 chunks: 128-chunk tiles already give 512 CTAs
+    assert lib.blake3_workspace_size(64 << 20) == 512 * 32
+    assert lib.blake3_workspace_size(19 << 20) == 152 * 32  # 19456 chunks / 128
+    assert lib.blake3_workspace_size(18 << 20) == 288 * 32  # 144 tiles of 128 < 152: 64-chunk tiles
+    # 4 GiB: 32768 tile CVs, then 32 group CVs
+    assert lib.blake3_workspace_size(1 << 32) == 32768 * 32 + 32 * 32
     assert lib.blake3_reduce_workspace_size(1024, 10) == 0
     assert lib.blake3_reduce_workspace_size(1025, 10) == 64
     assert lib.blake3_reduce_workspace_size(5, 1) == 3 * 32 + 32 + 32
@@ -119,3 +121,10 @@ def test_stream_and_xof_argument_errors(lib):
     lib.blake3_hasher_free(None)
     assert lib.blake3_keyed_hash_xof(FAKE, 10, None, FAKE, 32, None) == 1
     assert lib.blake3_keyed_hash_xof(FAKE, 10, KEY, None, 32, None) == 1
+
+
+def test_host_entry_argument_errors(lib):
+    out = ctypes.create_string_buffer(32)
+    assert lib.blake3_keyed_hash_host(FAKE, 10, None, out, None, 0, None) == 1
+    assert lib.blake3_keyed_hash_host(FAKE, 10, KEY, None, None, 0, None) == 1
+    assert lib.blake3_keyed_hash_host(None, 10, KEY, out, None, 0, None) == 1

@@ -35,7 +35,8 @@ def test_full_size_digest_and_samples(name):
     # sampled chunk CVs (first, last = the partial one for the ragged size, random)
     cvs = binding.blake3_keyed_chunk_cvs(dev, key)
     idx = sorted(set([0, nchunks - 1, nchunks // 2] + list(rng.integers(0, nchunks, 64))))
-    # sampled CTA subtree roots (256 chunks each)
+    # sampled CTA subtree roots (the default subtree size)
+    per_tile = 1 << binding.library().blake3_default_leaves_log2()
     roots = binding.blake3_keyed_tile_roots(dev, key)
     ntiles = roots.shape[0]
     tidx = sorted(set([0, ntiles - 1] + list(rng.integers(0, ntiles, 8))))
@@ -51,6 +52,6 @@ def test_full_size_digest_and_samples(name):
         assert bytes(cvs_h[i]) == oracle.chunk_cv(key, chunk, i), i
     for t in tidx:
         t = int(t)
-        part = host[t * 256 * 1024:(t + 1) * 256 * 1024]
-        assert bytes(roots_h[t]) == oracle.subtree_cv(part, key, t * 256), t
+        part = host[t * per_tile * 1024:(t + 1) * per_tile * 1024]
+        assert bytes(roots_h[t]) == oracle.subtree_cv(part, key, t * per_tile), t
     assert got == oracle.keyed_hash(host, key)

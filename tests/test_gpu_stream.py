@@ -105,3 +105,25 @@ def test_hasher_large_matches_one_shot():
     got = bytes(h.finalize().cpu().numpy())
     assert got == bytes(binding.blake3_keyed_hash(d, w.key()).cpu().numpy())
     assert got == oracle.keyed_hash(host, w.key())
+
+
+@pytest.mark.parametrize("length", [0, 1, 1024, 1025, (1 << 20) + 3, (9 << 20) + 777])
+@pytest.mark.parametrize("staging_mib", [0, 2, 4])
+def test_hash_from_host_memory(length, staging_mib):
+    """Host input copied in overlapping segments (pinned and pageable) == the oracle digest."""
+    host = workloads.uniform_bytes(length + 5, length)
+    pinned = torch.empty(length, dtype=torch.uint8, pin_memory=True)
+    pinned.copy_(host)
+    staging = None
+    if staging_mib:
+        staging = torch.empty(3328 + (staging_mib << 20), dtype=torch.uint8, device="cuda")
+    ref = oracle.keyed_hash(host, KEY)
+    assert binding.blake3_keyed_hash_host(pinned, KEY, staging) == ref
+    assert binding.blake3_keyed_hash_host(host, KEY, staging) == ref
+
+
+def test_hash_from_host_rejects_small_staging():
+    host = torch.zeros(5000, dtype=torch.uint8)
+    staging = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.B3GError):
+        binding.blake3_keyed_hash_host(host, KEY, staging)
