@@ -112,6 +112,21 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows), "samples": len(loaded), "reasons": reasons}
 
 
+def _traffic_per_launch(lib, nchunks):
+    """DRAM bytes of one leaf launch, scaled by chunks from the ncu capture recorded in
+    profiles/leaf_tma_kernel_traffic.json; None if that capture is of another kernel
+    configuration than the one built."""
+    p = os.path.join(HERE, "profiles", "leaf_tma_kernel_traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        rec = json.load(f)
+    if rec.get("kernel_config") != lib.blake3_kernel_config().decode():
+        return None, "capture is of another kernel configuration"
+    per_chunk = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) / rec["chunks"]
+    return per_chunk * nchunks, f"ncu capture on {rec['workload']} scaled by chunks ({rec['chunks']} -> {nchunks})"
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -276,6 +291,11 @@ def run_ours(args):
         "roofline_gbs": min(float(peaks.get("hbm_gbs", 6800.0)), int_peak / (ops / n) / 1e9),
     }
     roofline["frac_of_min_roofline"] = (n / leaf_s / 1e9) / roofline["roofline_gbs"]
+    traffic, traffic_src = _traffic_per_launch(lib, nchunks)
+    roofline["traffic"] = traffic
+    roofline["traffic_source"] = traffic_src
+    roofline["algorithmic_bytes"] = n
+    roofline["kernel_config"] = lib.blake3_kernel_config().decode()
 
     # end to end through the public call, host buffers, copies inside the timed region
     e2e = None
@@ -415,9 +435,24 @@ def run_mode(args):
         ms_graph = _timed(graph.replay, max(3, args.steps // per_graph), 2) / per_graph
         if bytes(out32.cpu().numpy()) != bytes(binding.blake3_keyed_hash(d, key).cpu().numpy()):
             raise RuntimeError("graph-replayed digest differs")
+        # the same with the fused final reduction (one launch + a 4-byte memset)
+        binding.blake3_set_option(binding.B3G_OPT_FUSED_FINAL, 1)
+        try:
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    binding.blake3_keyed_hash_ws(d, key, ws, out=out32)
+            torch.cuda.current_stream().wait_stream(s)
+            graph_f = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_f, stream=s):
+                for _ in range(per_graph):
+                    binding.blake3_keyed_hash_ws(d, key, ws, out=out32)
+            ms_fused = _timed(graph_f.replay, max(3, args.steps // per_graph), 2) / per_graph
+        finally:
+            binding.blake3_set_option(binding.B3G_OPT_FUSED_FINAL, 0)
         line = {"mode": "small", "metric": "GB/s hashed, 1 MiB input (keyed BLAKE3, 1 GB300)",
                 "value": d.numel() / ms_graph / 1e6, "unit": "GB/s", "us_per_digest_graph": ms_graph * 1e3,
                 "us_per_call_eager": ms_call * 1e3, "eager_GBps": d.numel() / ms_call / 1e6,
+                "us_per_digest_graph_fused_final": ms_fused * 1e3,
                 "config": {"workload": "1MiB uniform seed 0, key seed 1",
                            "graph": f"{per_graph} blake3_keyed_hash_ws calls per CUDA graph"}}
     print(json.dumps(line), flush=True)

@@ -29,6 +29,7 @@ _BINDING_NAMES = (
     "blake3_selftest_bounded_wait",
     "blake3_tile_count",
     "blake3_strerror",
+    "blake3_set_option",
     "B3GError",
     "library",
 )

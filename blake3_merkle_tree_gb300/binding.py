@@ -49,6 +49,8 @@ def library() -> ctypes.CDLL:
             "blake3_strerror": (ctypes.c_char_p, [i32]),
             "blake3_last_cuda_error": (ctypes.c_char_p, []),
             "blake3_default_leaves_log2": (i32, []),
+            "blake3_kernel_config": (ctypes.c_char_p, []),
+            "blake3_set_option": (i32, [i32, ctypes.c_int64]),
             "blake3_keyed_hash": (i32, [vp, u64, vp, vp, vp]),
             "blake3_workspace_size": (sz, [u64]),
             "blake3_keyed_hash_ws": (i32, [vp, u64, vp, vp, vp, sz, vp]),
@@ -301,3 +303,10 @@ def blake3_keyed_hash_host(data: torch.Tensor, key, staging: torch.Tensor | None
                                           st_ptr, st_bytes, _stream(stream))
     _check(st, "blake3_keyed_hash_host")
     return out.raw
+
+
+B3G_OPT_FUSED_FINAL = 1
+
+
+def blake3_set_option(option: int, value: int) -> None:
+    _check(library().blake3_set_option(option, value), "blake3_set_option")

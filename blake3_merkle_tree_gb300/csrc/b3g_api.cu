@@ -11,6 +11,7 @@
 //      launch with a single group sets ROOT.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -122,6 +123,8 @@ LeafArgs leaf_args(const void *d_in, uint64_t len, uint64_t chunk_offset, const 
     key_words(key, a.key);
     a.root = root ? 1u : 0u;
     a.tail_bytes = static_cast<uint32_t>(len % kChunkBytes);
+    a.ticket = nullptr;
+    a.final_out = nullptr;
     return a;
 }
 
@@ -141,6 +144,15 @@ int choose_leaves_log2(uint64_t n_chunks) {
     return t;
 }
 
+// The fused final reduction lives in the bulk-tensor-copy kernel; inputs that take
+// the plain-load kernel (misaligned, or no full chunk) use the reduction kernel.
+std::atomic<int> g_fused_final{0};
+
+bool fused_path(const void *d_in, uint64_t n_full) {
+    return g_fused_final.load(std::memory_order_relaxed) != 0 && n_full >= 1 &&
+           (reinterpret_cast<uintptr_t>(d_in) & 15u) == 0;
+}
+
 // The whole path: leaf kernel, then the reduction levels.  `ws` must hold
 // blake3_workspace_size(len) bytes when more than one tile exists.
 b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32], bool root,
@@ -155,6 +167,15 @@ b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, con
         return launch_leaf(a, t, false, stream);
     }
     a.out = ws;
+    if (a.n_tiles <= kMaxFusedTiles && fused_path(d_in, a.n_full)) {
+        // few tiles: the last CTA folds the tile CVs itself (one launch, no
+        // reduction kernel); its ticket counter sits after the tile CVs
+        a.ticket = reinterpret_cast<uint32_t *>(ws + round16(a.n_tiles * 32));
+        a.final_out = d_out32;
+        cudaError_t e = cudaMemsetAsync(a.ticket, 0, sizeof(uint32_t), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(ticket)");
+        return launch_leaf(a, t, false, stream);
+    }
     st = launch_leaf(a, t, false, stream);
     if (st != B3G_OK) return st;
     return reduce_levels(ws, a.n_tiles, a.key, root, kDefaultGroupLog2, d_out32,
@@ -165,7 +186,9 @@ size_t hash_workspace(uint64_t len) {
     const uint64_t n = n_chunks_of(len);
     const uint64_t tiles = ceil_div(n, 1ull << choose_leaves_log2(n));
     if (tiles == 1) return 0;
-    return round16(tiles * 32) + reduce_ws(tiles, kDefaultGroupLog2);
+    // the fused path needs 16 bytes for its ticket counter instead of reduction levels
+    const size_t levels = reduce_ws(tiles, kDefaultGroupLog2);
+    return round16(tiles * 32) + (tiles <= kMaxFusedTiles && levels < 16 ? 16 : levels);
 }
 
 // Runs hash_range with a stream-ordered temporary workspace.
@@ -222,6 +245,17 @@ const char *blake3_strerror(b3g_status s) {
 const char *blake3_last_cuda_error(void) { return g_last_cuda_error; }
 
 int blake3_default_leaves_log2(void) { return kDefaultLeavesLog2; }
+
+const char *blake3_kernel_config(void) { return kernel_config(); }
+
+b3g_status blake3_set_option(b3g_option option, int64_t value) {
+    switch (option) {
+        case B3G_OPT_FUSED_FINAL:
+            g_fused_final.store(value != 0 ? 1 : 0, std::memory_order_relaxed);
+            return B3G_OK;
+    }
+    return B3G_ERR_ARG;
+}
 
 size_t blake3_workspace_size(uint64_t len) { return hash_workspace(len); }
 

@@ -36,7 +36,15 @@ struct LeafArgs {
     uint32_t key[8];
     uint32_t root;        // ROOT on the final compression if the whole tree is one tile
     uint32_t tail_bytes;  // bytes of the partial last chunk; 0 if none
+    // Fused final reduction (at most 32 tiles): when `ticket` is not NULL (a zeroed
+    // counter), the reducer that finishes the last tile folds all tile CVs (in `out`)
+    // to the root, with ROOT when `root` is set, and writes it to `final_out`.
+    uint32_t *ticket;
+    uint8_t *final_out;
 };
+
+// Largest tile count the fused final reduction handles (one CV per lane of a warp).
+constexpr uint64_t kMaxFusedTiles = 32;
 
 // Arguments of the CV reduction kernel (page section "Kernel 2 和 3").
 struct ReduceArgs {
@@ -52,6 +60,9 @@ struct ReduceArgs {
 // Chooses the bulk-tensor-copy path when `in` is 16-byte aligned and holds at
 // least one full chunk, the plain-load path otherwise.
 b3g_status launch_leaf(const LeafArgs &args, int leaves_log2, bool chunk_cvs, cudaStream_t stream);
+
+// "leaf_tma_kernel<C,S,LOAD> unroll=.. min_blocks=.. g_form=.." of the default tile size.
+const char *kernel_config();
 
 // One level of CV reduction.
 b3g_status launch_reduce(const ReduceArgs &args, cudaStream_t stream);

@@ -32,6 +32,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdio>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -39,8 +40,23 @@
 #include "b3g_device.cuh"
 #include "b3g_internal.h"
 
+// Unroll factor of the consumer's copy loop (the copies of one chunk), and the
+// minimum resident CTAs per SM asked of the register allocator (0: none).
+#ifndef B3G_UNROLL
+#define B3G_UNROLL 1
+#endif
+#ifndef B3G_MIN_BLOCKS
+#define B3G_MIN_BLOCKS 0
+#endif
+#if B3G_MIN_BLOCKS > 0
+#define B3G_LEAF_BOUNDS(threads) __launch_bounds__(threads, B3G_MIN_BLOCKS)
+#else
+#define B3G_LEAF_BOUNDS(threads) __launch_bounds__(threads)
+#endif
+
 namespace b3g {
 
+constexpr int kCopyLoopUnroll = B3G_UNROLL;
 constexpr uint32_t kBarTree = 1;  // named barrier id of the consumer threads
 
 // ---------------------------------------------------------------------------------
@@ -86,8 +102,62 @@ struct TmaCfg {
     static_assert(S >= 2 && S <= kLoadsPerChunk, "stage count");
 };
 
+struct Words8 {
+    uint32_t w[8];
+};
+
+// CV of the partial last chunk (`bytes` < 1024, at least 1, starting at byte `off`),
+// read straight from global memory with bounds checks.  Only the one thread that owns
+// that chunk calls it, once, so it is kept out of line, away from the hot loop; all
+// arguments and the result travel by value so that no caller array escapes.
+__device__ __noinline__ Words8 partial_chunk_cv(const uint8_t *in, uint64_t len, uint64_t off, uint64_t ctr,
+                                                uint32_t bytes, uint32_t end_flags, Words8 key) {
+    const uint32_t nblocks = (bytes + 63u) / 64u;
+    Words8 cv = key;
+    for (uint32_t b = 0; b < nblocks; ++b) {
+        uint32_t m[16];
+        load_block_global(in, len, off + 64ull * b, m);
+        const bool last = b + 1 == nblocks;
+        const uint32_t flags = kKeyedHash | (b == 0 ? kChunkStart : 0u) | (last ? end_flags : 0u);
+        compress(cv.w, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32),
+                 last ? bytes - 64u * (nblocks - 1u) : 64u, flags);
+    }
+    return cv;
+}
+
+// Fused final reduction (at most 32 tiles, one tile per CTA).  Called by a whole
+// reducer warp right after its lane 0 stored the tile CV.  The warp that draws the
+// last ticket has seen every other tile CV published (each is stored, then fenced,
+// before its warp takes a ticket) and folds them with the warp-level tree, ROOT on
+// the final compression.  This replaces the separate reduction launch for small inputs.
+__device__ __forceinline__ void fused_final_reduce(const LeafArgs &a, const uint32_t key[8]) {
+    const uint32_t lane = threadIdx.x & 31u;
+    uint32_t ticket = 0;
+    if (lane == 0) {
+        __threadfence();
+        ticket = atomicAdd(a.ticket, 1u);
+    }
+    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+    const uint32_t n = static_cast<uint32_t>(a.n_tiles);
+    if (ticket != n - 1) return;
+    __threadfence();
+    uint32_t x[8];
+    if (lane < n) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(a.out + 32ull * lane);
+        const uint4 w0 = __ldcg(p), w1 = __ldcg(p + 1);
+        x[0] = w0.x; x[1] = w0.y; x[2] = w0.z; x[3] = w0.w;
+        x[4] = w1.x; x[5] = w1.y; x[6] = w1.z; x[7] = w1.w;
+    }
+    warp_tree(x, n, key, a.root != 0);
+    if (lane == 0) {
+        uint4 *o = reinterpret_cast<uint4 *>(a.final_out);
+        o[0] = make_uint4(x[0], x[1], x[2], x[3]);
+        o[1] = make_uint4(x[4], x[5], x[6], x[7]);
+    }
+}
+
 template <int C, int S, int LOAD, bool CHUNK_CVS>
-__global__ void __launch_bounds__(C + 32)
+__global__ void B3G_LEAF_BOUNDS(C + 32)
     leaf_tma_kernel(const __grid_constant__ CUtensorMap tmap, const LeafArgs a) {
     using Cfg = TmaCfg<C, S, LOAD, CHUNK_CVS>;
     extern __shared__ uint8_t smem_raw[];
@@ -167,6 +237,7 @@ __global__ void __launch_bounds__(C + 32)
                     o[0] = make_uint4(x[0], x[1], x[2], x[3]);
                     o[1] = make_uint4(x[4], x[5], x[6], x[7]);
                 }
+                if (a.ticket) fused_final_reduce(a, key);
             }
         }
         return;
@@ -176,24 +247,31 @@ __global__ void __launch_bounds__(C + 32)
     const uint32_t r = tid;
     const uint32_t ring = rings0 + warp * Cfg::kRingBytes;
     const uint32_t fullw = full0 + 8 * S * warp;
-    // 16-byte unit u of row `lane` sits at u ^ swz (TMA 128B / 64B swizzle)
+    // 16-byte unit u of row `lane` sits at u ^ swz (TMA 128B / 64B swizzle); the byte
+    // offsets of the row's units within a stage are fixed for the thread
     const uint32_t swz = LOAD == 128 ? (lane & 7u) : ((lane >> 1) & 3u);
-    const uint32_t row_off = lane * LOAD;
+    uint32_t unit_addr[LOAD / 16];
+#pragma unroll
+    for (int u = 0; u < LOAD / 16; ++u) unit_addr[u] = ring + lane * LOAD + ((static_cast<uint32_t>(u) ^ swz) << 4);
 
     // Copy stream of this warp: copy i brings part (i mod kLoadsPerChunk) of the warp's
-    // rows of tile blockIdx.x + (i / kLoadsPerChunk) * gridDim.x.  Only lane 0 issues.
-    uint64_t next_tile = blockIdx.x;
+    // 32 rows of the CTA's (i / kLoadsPerChunk)-th tile.  Only lane 0 issues.
+    const uint64_t my_tiles = a.n_tiles > blockIdx.x ? (a.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    uint32_t copies_left = static_cast<uint32_t>(my_tiles * Cfg::kLoadsPerChunk);
+    uint32_t next_row = static_cast<uint32_t>(blockIdx.x * C + Cfg::kRowsPerCopy * warp);
+    const uint32_t row_step = gridDim.x * C;
     uint32_t next_part = 0;
     uint32_t issued = 0, consumed = 0;
     auto issue = [&](uint32_t stage) {
-        if (next_tile >= a.n_tiles) return;
+        if (copies_left == 0) return;
+        --copies_left;
         mbar_arrive_expect_tx(fullw + 8 * stage, Cfg::kStageBytes);
         tma_load_2d(ring + stage * Cfg::kStageBytes, &tmap, static_cast<int32_t>(next_part * (LOAD / 4)),
-                    static_cast<int32_t>(next_tile * C + Cfg::kRowsPerCopy * warp), fullw + 8 * stage);
+                    static_cast<int32_t>(next_row), fullw + 8 * stage);
         ++issued;
         if (++next_part == Cfg::kLoadsPerChunk) {
             next_part = 0;
-            next_tile += gridDim.x;
+            next_row += row_step;
         }
     };
     if (lane == 0) {
@@ -201,68 +279,77 @@ __global__ void __launch_bounds__(C + 32)
         for (int i = 0; i < S; ++i) issue(static_cast<uint32_t>(i));
     }
 
-    uint32_t s = 0, ph = 0;  // stage of the next copy to consume and its fill parity
+    // When S divides the copies per chunk every chunk starts at stage 0, so a copy's
+    // stage and fill parity follow from its position in the chunk (and the loop may be
+    // unrolled so that stage addresses become immediates).
+    constexpr bool kStageFromPos = Cfg::kLoadsPerChunk % S == 0;
+    uint32_t s = 0, ph = 0;  // otherwise: stage of the next copy and its fill parity
     uint32_t k = 0;
     bool aborted = false;
 
     for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
         const uint64_t chunk = tile * C + r;
         const bool valid = chunk < a.n_chunks;
-        const bool is_tail = a.tail_bytes != 0 && chunk == a.n_full;
-        const uint32_t nblocks = is_tail ? (a.tail_bytes + 63u) / 64u : 16u;
-        const uint32_t last_len = is_tail ? a.tail_bytes - 64u * (nblocks - 1u) : 64u;
         const uint64_t ctr = a.counter_base + chunk;
         const uint32_t ctr_lo = static_cast<uint32_t>(ctr);
         const uint32_t ctr_hi = static_cast<uint32_t>(ctr >> 32);
         const uint32_t end_flags = kChunkEnd | ((a.root && a.n_chunks == 1) ? kRoot : 0u);
+        const uint32_t tile_par = (k * (Cfg::kLoadsPerChunk / S)) & 1u;  // used when kStageFromPos
 
+        // Every thread compresses its row as a full chunk; the owner of the partial
+        // last chunk (its row reads as zeros) redoes its chunk after the loop.
         uint32_t cv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) cv[i] = key[i];
+        uint32_t flags = kKeyedHash | kChunkStart;
 
-#pragma unroll 1
+#pragma unroll kCopyLoopUnroll
         for (int ld = 0; ld < Cfg::kLoadsPerChunk; ++ld) {
-            if (!mbar_wait_bounded(fullw + 8 * s, ph, a.wait_limit_ns)) {
+            const uint32_t st = kStageFromPos ? static_cast<uint32_t>(ld % S) : s;
+            const uint32_t par = kStageFromPos ? (tile_par ^ (static_cast<uint32_t>(ld / S) & 1u)) : ph;
+            if (!mbar_wait_bounded(fullw + 8 * st, par, a.wait_limit_ns)) {
                 atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
                 aborted = true;
                 break;
             }
-            const uint32_t rowp = ring + s * Cfg::kStageBytes + row_off;
+            const uint32_t stage_off = st * Cfg::kStageBytes;
 #pragma unroll
             for (int j = 0; j < Cfg::kBlocksPerLoad; ++j) {
-                const uint32_t b = ld * Cfg::kBlocksPerLoad + j;
+                const int b = ld * Cfg::kBlocksPerLoad + j;
                 uint32_t m[16];
-                if (!is_tail) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t u = static_cast<uint32_t>(4 * j + q);
-                        const uint4 w = lds128(rowp + ((u ^ swz) << 4));
-                        m[4 * q + 0] = w.x;
-                        m[4 * q + 1] = w.y;
-                        m[4 * q + 2] = w.z;
-                        m[4 * q + 3] = w.w;
-                    }
-                } else {
-                    load_block_global(a.in, a.len, chunk * kChunkBytes + 64ull * b, m);
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w = lds128(unit_addr[4 * j + q] + stage_off);
+                    m[4 * q + 0] = w.x;
+                    m[4 * q + 1] = w.y;
+                    m[4 * q + 2] = w.z;
+                    m[4 * q + 3] = w.w;
                 }
-                const bool last = b + 1 == nblocks;
-                const uint32_t flags = kKeyedHash | (b == 0 ? kChunkStart : 0u) | (last ? end_flags : 0u);
-                if (b < nblocks) compress(cv, m, ctr_lo, ctr_hi, last ? last_len : 64u, flags);
+                compress(cv, m, ctr_lo, ctr_hi, 64u, b == 15 ? (flags | end_flags) : flags);
+                flags = kKeyedHash;
             }
-            // every lane has consumed stage s (its words went into the compression):
+            // every lane has consumed stage st (its words went into the compression):
             // refill it with the copy S positions ahead
             __syncwarp();
             ++consumed;
             if (lane == 0) {
                 fence_proxy_async_smem();
-                issue(s);
+                issue(st);
             }
-            if (++s == S) {
+            if (!kStageFromPos && ++s == S) {
                 s = 0;
                 ph ^= 1u;
             }
         }
         if (aborted) break;
+        if (a.tail_bytes != 0 && chunk == a.n_full) {
+            Words8 k8, t;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) k8.w[i] = key[i];
+            t = partial_chunk_cv(a.in, a.len, chunk * kChunkBytes, ctr, a.tail_bytes, end_flags, k8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cv[i] = t.w[i];
+        }
 
         if constexpr (CHUNK_CVS) {
             if (valid) {
@@ -511,6 +598,17 @@ b3g_status launch_c(const LeafArgs &a, bool chunk_cvs, bool tma, cudaStream_t st
 }
 
 }  // namespace
+
+const char *kernel_config() {
+    static char buf[160];
+    static std::once_flag once;
+    std::call_once(once, [] {
+        std::snprintf(buf, sizeof buf, "leaf_tma_kernel<%d,%d,%d> unroll=%d min_blocks=%d g_form=%d",
+                      1 << kDefaultLeavesLog2, Tuning<(1 << kDefaultLeavesLog2)>::S,
+                      Tuning<(1 << kDefaultLeavesLog2)>::LOAD, kCopyLoopUnroll, B3G_MIN_BLOCKS, B3G_G_FORM);
+    });
+    return buf;
+}
 
 b3g_status launch_leaf(const LeafArgs &a, int leaves_log2, bool chunk_cvs, cudaStream_t stream) {
     int dev = 0;

@@ -104,6 +104,8 @@ extern "C" b3g_status blake3_keyed_hash_noalloc(const void *d_in, uint64_t len, 
                    (static_cast<uint32_t>(key[4 * i + 2]) << 16) | (static_cast<uint32_t>(key[4 * i + 3]) << 24);
     a.root = 1;
     a.tail_bytes = static_cast<uint32_t>(len % kChunkBytes);
+    a.ticket = nullptr;
+    a.final_out = nullptr;
     if (tiles == 1) {
         a.out = d_out32;
         return launch_leaf(a, t, false, s);

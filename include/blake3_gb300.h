@@ -75,6 +75,26 @@ const char *blake3_last_cuda_error(void);
 /* Chunks per CTA subtree used when leaves_log2 is -1 (a power of two: 2^7 = 128). */
 int blake3_default_leaves_log2(void);
 
+/* Library-wide options (process-wide, thread-safe to set; they apply to calls made
+ * after the change). */
+typedef enum {
+    /* 0 (default) or 1.  With 1, an input of at most 32 CTA subtrees is reduced to its
+     * digest by the CTA that finishes last (an atomic ticket counter, zeroed by a 4-byte
+     * memset on the stream) instead of by a second kernel launch.  Measured on GB300 it
+     * is slower for 1 MiB (24.6 vs 22.5 us per digest in a CUDA graph): the memset costs
+     * more than the launch it saves.  Applies to 16-byte aligned inputs with at least
+     * one full chunk. */
+    B3G_OPT_FUSED_FINAL = 1,
+} b3g_option;
+
+/* Sets an option.  Errors: B3G_ERR_ARG (unknown option). */
+b3g_status blake3_set_option(b3g_option option, int64_t value);
+
+/* Static text naming the compiled configuration of the leaf kernel for the default
+ * subtree size, e.g. "leaf_tma_kernel<128,3,64> unroll=1 min_blocks=0 g_form=3"
+ * (chunks per CTA, stages per consumer warp, bytes per copy, build options). */
+const char *blake3_kernel_config(void);
+
 /*
  * blake3_keyed_hash -- the digest of d_in[0..len) under `key`, written to d_out32.
  * Page sections "BLAKE3" (chunking, tree rules), "Kernel 1" (leaf kernel with the

@@ -57,9 +57,10 @@ def test_sizes(lib):
     assert lib.blake3_tile_count(1 << 20, 4) == 0
     assert lib.blake3_workspace_size(0) == 0  # one chunk, one tile: no workspace
     assert lib.blake3_workspace_size(32 * 1024) == 0  # 32 chunks fit one 32-chunk tile
-    # small inputs spread over 32-chunk tiles: 1 MiB = 1024 chunks = 32 tiles
-    assert lib.blake3_workspace_size(1 << 20) == 32 * 32
-    assert lib.blake3_workspace_size(256 * 1024) == 8 * 32
+    # small inputs spread over 32-chunk tiles: 1 MiB = 1024 chunks = 32 tiles, reduced by
+    # the last CTA (16 bytes for its ticket counter)
+    assert lib.blake3_workspace_size(1 << 20) == 32 * 32 + 16
+    assert lib.blake3_workspace_size(256 * 1024) == 8 * 32 + 16
     # 64 MiB = 65536 chunks: 128-chunk tiles already give 512 CTAs
     assert lib.blake3_workspace_size(64 << 20) == 512 * 32
     assert lib.blake3_workspace_size(19 << 20) == 152 * 32  # 19456 chunks / 128
@@ -128,3 +129,9 @@ def test_host_entry_argument_errors(lib):
     assert lib.blake3_keyed_hash_host(FAKE, 10, None, out, None, 0, None) == 1
     assert lib.blake3_keyed_hash_host(FAKE, 10, KEY, None, None, 0, None) == 1
     assert lib.blake3_keyed_hash_host(None, 10, KEY, out, None, 0, None) == 1
+
+
+def test_options_and_config(lib):
+    assert lib.blake3_set_option(99, 1) == 6
+    assert lib.blake3_set_option(1, 0) == 0
+    assert lib.blake3_kernel_config().startswith(b"leaf_tma_kernel<")

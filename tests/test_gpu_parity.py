@@ -173,3 +173,23 @@ def test_generator_same_bytes_on_gpu_and_cpu():
         a = workloads.uniform_bytes(seed, n, device="cuda").cpu()
         b = workloads.uniform_bytes(seed, n)
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("length", [2 * 1024, 33 * 1024 + 5, 300 * 1024 + 3, (1 << 20), (1 << 20) + 1,
+                                    4 * 128 * 1024 * 8 - 7])
+def test_fused_final_reduction_option(length):
+    """With the fused-final option the last CTA reduces the tile CVs itself."""
+    host = workloads.uniform_bytes(length + 9, length)
+    d = host.cuda()
+    ref = oracle.keyed_hash(host, KEY)
+    binding.blake3_set_option(binding.B3G_OPT_FUSED_FINAL, 1)
+    try:
+        for _ in range(2):  # the ticket must be re-zeroed on every call
+            assert bytes(binding.blake3_keyed_hash(d, KEY).cpu().numpy()) == ref
+        ws = torch.empty(binding.blake3_workspace_size(length), dtype=torch.uint8, device="cuda")
+        ws.fill_(0xAB)  # a dirty workspace
+        assert bytes(binding.blake3_keyed_hash_ws(d, KEY, ws).cpu().numpy()) == ref
+        assert bytes(binding.blake3_keyed_subtree_root(d, KEY, 0, False).cpu().numpy()) == \
+            oracle.subtree_cv(host, KEY, 0, False)
+    finally:
+        binding.blake3_set_option(binding.B3G_OPT_FUSED_FINAL, 0)
