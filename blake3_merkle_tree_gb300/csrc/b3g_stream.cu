@@ -105,7 +105,11 @@ enum RecordMode : uint32_t {
     kRecFinalize = 2,  // root record of the whole input (stack untouched)
     kRecMerge = 3,     // merge the stack to `target`
     kRecParent = 4,    // record = (key, message words already in place, 64, KEYED_HASH|PARENT)
+    kRecPushMany = 5,  // for each piece in order: merge to popcount(position), push its root
 };
+
+constexpr int kMaxPieces = 96;        // pieces of one update on the batched path
+constexpr int kMaxSmallPieces = 16;   // pieces shorter than one CTA subtree (head and tail)
 
 struct RecordArgs {
     const uint8_t *in;  // kRecChunk: the chunk bytes
@@ -116,6 +120,10 @@ struct RecordArgs {
     uint32_t target;    // stack entries after merging (kRecPush, kRecMerge)
     uint32_t mode;
     uint32_t key[8];
+    // kRecPushMany: roots of `npieces` pieces (32 bytes each) and their chunk positions
+    const uint8_t *roots;
+    uint32_t npieces;
+    uint64_t piece_pos[kMaxPieces];
 };
 
 // The sequential bookkeeping of the hasher on one thread: at most 65 merges and one
@@ -139,6 +147,16 @@ __global__ void record_kernel(const RecordArgs a) {
             uint32_t cv[8];
             chunk_cv(buf, 1024u, a.pushed, key, cv);
             for (int i = 0; i < 8; ++i) stack[8 * d + i] = cv[i];
+            return;
+        }
+        case kRecPushMany: {
+            uint32_t d = a.depth;
+            for (uint32_t j = 0; j < a.npieces; ++j) {
+                d = merge_down(stack, d, static_cast<uint32_t>(__popcll(a.piece_pos[j])), key);
+                const uint32_t *rw = reinterpret_cast<const uint32_t *>(a.roots + 32ull * j);
+                for (int i = 0; i < 8; ++i) stack[8 * d + i] = rw[i];
+                ++d;
+            }
             return;
         }
         case kRecParent:
@@ -177,6 +195,96 @@ __global__ void record_kernel(const RecordArgs a) {
         }
         default:
             return;
+    }
+}
+
+// Small pieces (at most 64 full chunks each, counters from `counter`), one CTA per
+// piece, plain loads (any alignment): root of each piece (a perfect subtree, no ROOT).
+struct PiecesArgs {
+    const uint8_t *base;  // piece j starts at base + off[j]
+    uint8_t *out;         // root of piece j at out + 32 * slot[j]
+    uint32_t key[8];
+    uint64_t off[kMaxSmallPieces];
+    uint64_t counter[kMaxSmallPieces];
+    uint32_t nchunks[kMaxSmallPieces];
+    uint32_t slot[kMaxSmallPieces];
+};
+
+__global__ void __launch_bounds__(64) pieces_kernel(const PiecesArgs a) {
+    __shared__ __align__(128) uint8_t node_mem[64 * 32];
+    const uint32_t nodes = smem_u32(node_mem);
+    const uint32_t j = blockIdx.x, r = threadIdx.x;
+    const uint32_t cnt = a.nchunks[j];
+    uint32_t key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) key[i] = a.key[i];
+    if (r < cnt) {
+        const uint8_t *p = a.base + a.off[j] + 1024ull * r;
+        const uint64_t ctr = a.counter[j] + r;
+        uint32_t cv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cv[i] = key[i];
+#pragma unroll 1
+        for (uint32_t b = 0; b < 16; ++b) {
+            uint32_t m[16];
+            load_block_global(p, 1024, 64ull * b, m);
+            const uint32_t flags = kKeyedHash | (b == 0 ? kChunkStart : 0u) | (b == 15 ? kChunkEnd : 0u);
+            compress(cv, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32), 64u, flags);
+        }
+        store_node(nodes, r, cv);
+    }
+    named_bar_sync(1, 64);
+    uint32_t root[8];
+    block_tree(nodes, cnt, r, 64, 1, key, false, root);
+    if (r == 0) {
+        uint4 *o = reinterpret_cast<uint4 *>(a.out + 32ull * a.slot[j]);
+        o[0] = make_uint4(root[0], root[1], root[2], root[3]);
+        o[1] = make_uint4(root[4], root[5], root[6], root[7]);
+    }
+}
+
+// Each CTA reduces one range of `count` CVs (a power of two, at most 1024: a perfect
+// subtree) starting at in + 32 * start, to out + 32 * slot (no ROOT).
+struct RangesArgs {
+    const uint8_t *in;
+    uint8_t *out;
+    uint32_t key[8];
+    uint32_t start[kMaxPieces];
+    uint32_t count[kMaxPieces];
+    uint32_t slot[kMaxPieces];
+};
+
+__global__ void __launch_bounds__(512) ranges_reduce_kernel(const RangesArgs a) {
+    __shared__ __align__(128) uint8_t node_mem[512 * 32];
+    const uint32_t nodes = smem_u32(node_mem);
+    const uint32_t j = blockIdx.x, tid = threadIdx.x;
+    uint32_t key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) key[i] = a.key[i];
+    const uint32_t m = a.count[j];
+    const uint8_t *in = a.in + 32ull * a.start[j];
+    const uint32_t half = m >> 1;
+    if (tid < half) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(in + 64ull * tid);
+        const uint4 w0 = p[0], w1 = p[1], w2 = p[2], w3 = p[3];
+        uint32_t l[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        uint32_t r[8] = {w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+        uint32_t res[8];
+        parent(key, l, r, false, res);
+        store_node(nodes, tid, res);
+    } else if (m == 1 && tid == 0) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(in);
+        const uint4 w0 = p[0], w1 = p[1];
+        uint32_t res[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        store_node(nodes, 0, res);
+    }
+    named_bar_sync(1, blockDim.x);
+    uint32_t root[8];
+    block_tree(nodes, m == 1 ? 1u : half, tid, blockDim.x, 1, key, false, root);
+    if (tid == 0) {
+        uint4 *o = reinterpret_cast<uint4 *>(a.out + 32ull * a.slot[j]);
+        o[0] = make_uint4(root[0], root[1], root[2], root[3]);
+        o[1] = make_uint4(root[4], root[5], root[6], root[7]);
     }
 }
 
@@ -292,26 +400,33 @@ struct b3g_hasher {
 
 namespace {
 
-// Push the chunks [h->pushed, h->pushed + nchunks) that start at `p` as aligned
-// power-of-two subtrees.
-b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStream_t s) {
-    struct Piece {
-        uint64_t pos, size;
-    };
+// The aligned power-of-two pieces of the chunk run [pos, pos + n): at every position
+// the largest power of two that divides the position and fits; a piece that starts at
+// chunk 0 is split into its two halves, so that the root's children stay separate.
+struct Piece {
+    uint64_t pos, size;
+};
+
+std::vector<Piece> decompose(uint64_t pos, uint64_t n) {
     std::vector<Piece> pieces;
-    uint64_t pos = h->pushed, left = nchunks;
-    while (left > 0) {
+    while (n > 0) {
         uint64_t size = 1;
-        while (size * 2 <= left && (pos == 0 || (pos % (size * 2)) == 0)) size *= 2;
-        if (pos == 0 && size >= 2) {  // keep the halves of a subtree starting at 0
+        while (size * 2 <= n && (pos == 0 || (pos % (size * 2)) == 0)) size *= 2;
+        if (pos == 0 && size >= 2) {
             pieces.push_back({0, size / 2});
             pieces.push_back({size / 2, size / 2});
         } else {
             pieces.push_back({pos, size});
         }
         pos += size;
-        left -= size;
+        n -= size;
     }
+    return pieces;
+}
+
+// One piece at a time: a subtree launch per piece and a merge launch before each push.
+b3g_status push_pieces_one_by_one(b3g_hasher *h, const uint8_t *p, const std::vector<Piece> &pieces,
+                                  cudaStream_t s) {
     uint64_t biggest = 0;
     for (const Piece &pc : pieces) biggest = pc.size > biggest ? pc.size : biggest;
     const size_t ws_bytes = blake3_workspace_size(biggest * kChunkBytes);
@@ -346,6 +461,134 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
         cudaError_t e = cudaFreeAsync(ws, s);
         if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
     }
+    return st;
+}
+
+// Push the chunks [h->pushed, h->pushed + nchunks) that start at `p`.  Batched: the
+// pieces shorter than a CTA subtree (only at the two ends of the run) go through one
+// launch of pieces_kernel; the longer pieces are contiguous and aligned to a CTA
+// subtree, so one leaf launch over their union yields their tile CVs, and one launch of
+// ranges_reduce_kernel (plus the ordinary reduction for pieces of more than 1024
+// tiles) turns those into piece roots; one record_kernel launch then does every merge
+// and push in order.
+b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStream_t s) {
+    const std::vector<Piece> pieces = decompose(h->pushed, nchunks);
+    const uint64_t tile = 1ull << kDefaultLeavesLog2;
+    const uint64_t base = h->pushed;
+    std::vector<size_t> small, big;
+    for (size_t j = 0; j < pieces.size(); ++j) (pieces[j].size < tile ? small : big).push_back(j);
+    uint64_t A = 0, B = 0;
+    if (!big.empty()) {
+        A = pieces[big.front()].pos;
+        B = pieces[big.back()].pos + pieces[big.back()].size;
+    }
+    uint64_t big_sum = 0;
+    for (size_t j : big) big_sum += pieces[j].size;
+    if (pieces.size() > static_cast<size_t>(kMaxPieces) || small.size() > static_cast<size_t>(kMaxSmallPieces) ||
+        big_sum != B - A || h->depth + pieces.size() >= static_cast<size_t>(kStackSlots) ||
+        (B - A) / tile > 0xffffffffull)
+        return push_pieces_one_by_one(h, p, pieces, s);
+
+    // scratch: piece roots, tile CVs of [A, B), workspace of the large-piece reductions
+    const uint64_t tiles = (B - A) / tile;
+    size_t huge_ws = 0;
+    for (size_t j : big) {
+        const uint64_t t = pieces[j].size / tile;
+        if (t > 1024) {
+            const size_t w = blake3_reduce_workspace_size(t, 10);
+            huge_ws = w > huge_ws ? w : huge_ws;
+        }
+    }
+    const size_t roots_bytes = (pieces.size() * 32 + 255) & ~size_t(255);
+    const size_t tiles_bytes = (tiles * 32 + 255) & ~size_t(255);
+    uint8_t *scratch = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), roots_bytes + tiles_bytes + huge_ws + 256, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
+    uint8_t *roots = scratch;
+    uint8_t *tile_cvs = scratch + roots_bytes;
+    uint8_t *huge = tile_cvs + tiles_bytes;
+    b3g_status st = B3G_OK;
+
+    if (!small.empty()) {
+        PiecesArgs pa;
+        std::memset(&pa, 0, sizeof pa);
+        pa.base = p;
+        pa.out = roots;
+        std::memcpy(pa.key, h->kw, sizeof pa.key);
+        for (size_t i = 0; i < small.size(); ++i) {
+            const Piece &pc = pieces[small[i]];
+            pa.off[i] = (pc.pos - base) * kChunkBytes;
+            pa.counter[i] = pc.pos;
+            pa.nchunks[i] = static_cast<uint32_t>(pc.size);
+            pa.slot[i] = static_cast<uint32_t>(small[i]);
+        }
+        pieces_kernel<<<static_cast<unsigned>(small.size()), 64, 0, s>>>(pa);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) st = cuda_fail(e, "pieces_kernel launch");
+    }
+    if (st == B3G_OK && !big.empty()) {
+        uint32_t *status = nullptr;
+        st = device_status_word(&status);
+        if (st == B3G_OK) {
+            LeafArgs a;
+            std::memset(&a, 0, sizeof a);
+            a.in = p + (A - base) * kChunkBytes;
+            a.len = (B - A) * kChunkBytes;
+            a.n_chunks = a.n_full = B - A;
+            a.counter_base = A;
+            a.n_tiles = tiles;
+            a.out = tile_cvs;
+            a.status = status;
+            a.wait_limit_ns = kWaitLimitNs;
+            std::memcpy(a.key, h->kw, sizeof a.key);
+            st = launch_leaf(a, kDefaultLeavesLog2, false, s);
+        }
+        RangesArgs ra;
+        std::memset(&ra, 0, sizeof ra);
+        ra.in = tile_cvs;
+        ra.out = roots;
+        std::memcpy(ra.key, h->kw, sizeof ra.key);
+        uint32_t nr = 0, widest = 1;
+        for (size_t j : big) {
+            if (st != B3G_OK) break;
+            const uint64_t t0 = (pieces[j].pos - A) / tile, t = pieces[j].size / tile;
+            if (t > 1024) {  // a very large piece: the ordinary multi-level reduction
+                st = blake3_keyed_reduce_cvs(tile_cvs + 32 * t0, t, h->key, 0, 10, roots + 32 * j, huge, huge_ws,
+                                             reinterpret_cast<b3g_stream_t>(s));
+                continue;
+            }
+            ra.start[nr] = static_cast<uint32_t>(t0);
+            ra.count[nr] = static_cast<uint32_t>(t);
+            ra.slot[nr] = static_cast<uint32_t>(j);
+            widest = static_cast<uint32_t>(t) > widest ? static_cast<uint32_t>(t) : widest;
+            ++nr;
+        }
+        if (st == B3G_OK && nr) {
+            const unsigned threads = widest / 2 < 32 ? 32 : widest / 2;
+            ranges_reduce_kernel<<<nr, threads, 0, s>>>(ra);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) st = cuda_fail(e, "ranges_reduce_kernel launch");
+        }
+    }
+    if (st == B3G_OK) {
+        RecordArgs rec = record_args(h->state, h->kw, kRecPushMany);
+        rec.depth = h->depth;
+        rec.roots = roots;
+        rec.npieces = static_cast<uint32_t>(pieces.size());
+        uint32_t d = h->depth;
+        for (size_t j = 0; j < pieces.size(); ++j) {
+            rec.piece_pos[j] = pieces[j].pos;
+            const uint32_t target = popcount64(pieces[j].pos);
+            d = (d > target ? target : d) + 1;
+        }
+        st = launch_record(rec, s);
+        if (st == B3G_OK) {
+            h->depth = d;
+            h->pushed = base + nchunks;
+        }
+    }
+    e = cudaFreeAsync(scratch, s);
+    if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
     return st;
 }
 
