@@ -17,20 +17,25 @@
 //     power-of-two left subtree and the rest; both are ordinary subtree roots.
 //
 // Streaming hasher: input arrives in device segments of any length.  A small device
-// state holds a stack of subtree CVs and the bytes of an unfinished chunk; the host
-// tracks the counts.
-//   - Every complete chunk is pushed, except while the input is at most one chunk
-//     (that chunk may turn out to be the whole input and then needs ROOT).
+// state holds a stack of subtree CVs; bytes not yet pushed wait in an accumulation
+// buffer (1024 bytes inside the state, later an own 64 MiB buffer); the host tracks
+// the counts.
+//   - Segments are copied into the buffer while they fit.  When one does not, the
+//     buffer's chunks are pushed, and so are the segment's whole chunks if they do not
+//     fit in the buffer either; what is left is kept.  Nothing is pushed while the
+//     input is at most one chunk (that chunk may turn out to be the whole input and
+//     then needs ROOT).
 //   - Whole runs of chunks are pushed as aligned power-of-two subtrees computed by
 //     the ordinary leaf and reduction kernels; a subtree pushed at position 0 is
 //     pushed as its two halves, so that the root's two children always exist.
 //   - Before pushing at chunk position p the stack is merged down to popcount(p)
 //     entries (the binary decomposition of p), so merges happen only once it is
 //     known that more input follows.
-//   - Finalize works on a copy of the stack: the unfinished chunk is appended, the
-//     copy is merged down to max(2, popcount(n)) entries and folded right to left;
-//     the bottom entry and the fold are the root's children.  The hasher can keep
-//     absorbing input afterwards.
+//   - Finalize works on a copy of the stack: the buffered chunks but the last are
+//     pushed onto it, the last (possibly partial) chunk is appended, the copy is
+//     merged down to max(2, popcount(n)) entries and folded right to left; the bottom
+//     entry and the fold are the root's children.  The hasher can keep absorbing
+//     input afterwards.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -101,8 +106,8 @@ __device__ uint32_t merge_down(uint32_t *st, uint32_t depth, uint32_t target, co
 
 enum RecordMode : uint32_t {
     kRecChunk = 0,     // root record of the single chunk at `in`
-    kRecPush = 1,      // merge the stack to `target`, push the CV of the buffered full chunk
-    kRecFinalize = 2,  // root record of the whole input (stack untouched)
+    kRecPush = 1,      // merge the stack to `target`, push the CV of the full chunk at `in`
+    kRecFinalize = 2,  // root record of the whole input, last chunk at `in` (stack untouched)
     kRecMerge = 3,     // merge the stack to `target`
     kRecParent = 4,    // record = (key, message words already in place, 64, KEYED_HASH|PARENT)
     kRecPushMany = 5,  // for each piece in order: merge to popcount(position), push its root
@@ -112,7 +117,7 @@ constexpr int kMaxPieces = 96;        // pieces of one update on the batched pat
 constexpr int kMaxSmallPieces = 16;   // pieces shorter than one CTA subtree (head and tail)
 
 struct RecordArgs {
-    const uint8_t *in;  // kRecChunk: the chunk bytes
+    const uint8_t *in;  // the chunk bytes (kRecChunk, kRecPush, kRecFinalize)
     uint8_t *state;     // hasher state, or a scratch area laid out the same way
     uint64_t pushed;    // chunks whose CVs are in the stack (= counter of the next chunk)
     uint32_t len;       // bytes of the chunk to finish (kRecChunk, kRecPush, kRecFinalize)
@@ -134,7 +139,6 @@ __global__ void record_kernel(const RecordArgs a) {
     for (int i = 0; i < 8; ++i) key[i] = a.key[i];
     uint32_t *stack = reinterpret_cast<uint32_t *>(a.state);
     uint32_t *rec = reinterpret_cast<uint32_t *>(a.state + kRecordOff);
-    const uint8_t *buf = a.state + kBufOff;
     switch (a.mode) {
         case kRecChunk:
             chunk_record(a.in, a.len, a.pushed, key, rec);
@@ -145,7 +149,7 @@ __global__ void record_kernel(const RecordArgs a) {
         case kRecPush: {
             const uint32_t d = merge_down(stack, a.depth, a.target, key);
             uint32_t cv[8];
-            chunk_cv(buf, 1024u, a.pushed, key, cv);
+            chunk_cv(a.in, 1024u, a.pushed, key, cv);
             for (int i = 0; i < 8; ++i) stack[8 * d + i] = cv[i];
             return;
         }
@@ -171,7 +175,7 @@ __global__ void record_kernel(const RecordArgs a) {
             uint64_t n = a.pushed;
             if (a.len > 0) {  // the unfinished chunk becomes the last leaf
                 d = merge_down(st, d, static_cast<uint32_t>(__popcll(n)), key);
-                chunk_cv(buf, a.len, n, key, st + 8 * d);
+                chunk_cv(a.in, a.len, n, key, st + 8 * d);
                 ++d;
                 ++n;
             }
@@ -363,21 +367,25 @@ b3g_status check_device(int want) {
     return dev == want ? B3G_OK : B3G_ERR_ARG;
 }
 
-// One non-blocking copy stream per device for blake3_keyed_hash_host, created on
-// first use and kept for the life of the process.
-b3g_status copy_stream(cudaStream_t *out) {
+// Per-device streams kept for the life of the process, created on first use: kind 0
+// carries the staging copies of blake3_keyed_hash_host, kind 1 is the side stream of
+// its hasher (created with the highest priority, like a hasher's own side stream).
+b3g_status cached_stream(int kind, cudaStream_t *out) {
     static std::mutex mu;
-    static cudaStream_t cache[64] = {};
+    static cudaStream_t cache[2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) return B3G_ERR_ARG;
+    if (dev < 0 || dev >= 64 || kind < 0 || kind > 1) return B3G_ERR_ARG;
     std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
-        e = cudaStreamCreateWithFlags(&cache[dev], cudaStreamNonBlocking);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
+    if (!cache[kind][dev]) {
+        int least = 0, greatest = 0;
+        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e == cudaSuccess)
+            e = cudaStreamCreateWithPriority(&cache[kind][dev], cudaStreamNonBlocking, kind == 1 ? greatest : least);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithPriority");
     }
-    *out = cache[dev];
+    *out = cache[kind][dev];
     return B3G_OK;
 }
 
@@ -387,18 +395,99 @@ b3g_status copy_stream(cudaStream_t *out) {
 using namespace b3g;
 
 // Host object of a streaming hasher (opaque to callers).
+//
+// Bytes absorbed but not yet pushed live in `acc`: at first the 1024-byte buffer inside
+// the state, then (on the first update that would otherwise start a push for a segment
+// shorter than kAccBytes) an own kAccBytes buffer, so that a stream of small segments
+// costs one device copy each and the chunks are pushed in large batches.  Work that
+// needs no SM-wide parallelism (small pieces, range reductions, the sequential stack
+// records) runs on the high-priority side stream `aux`, ordered against the caller's
+// stream with events, so that it overlaps the leaf launches on the caller's stream.
 struct b3g_hasher {
     uint8_t key[32];
     uint32_t kw[8];
-    uint8_t *state;    // device: stack, chunk buffer, root record
+    uint8_t *state;     // device: stack, 1024-byte chunk buffer, root record
+    uint8_t *acc;       // device: bytes absorbed but not pushed (the state's buffer or own)
+    uint64_t acc_cap;   // capacity of acc: 1024, or kAccBytes once grown
+    uint64_t acc_len;   // bytes in acc
+    bool may_grow;      // may switch acc to an own kAccBytes buffer
+    bool own_streams;   // aux and the events belong to this object
+    bool read_pending;  // aux has reads of a segment or of acc that the caller's stream has not waited for
     int device;
-    uint64_t count;    // bytes absorbed
-    uint64_t pushed;   // chunks whose CVs are represented in the stack
-    uint32_t depth;    // stack entries
-    uint32_t buf_len;  // bytes of the unfinished chunk in the buffer
+    uint64_t count;     // bytes absorbed
+    uint64_t pushed;    // chunks whose CVs are represented in the stack
+    uint32_t depth;     // stack entries
+    cudaStream_t aux;   // side stream
+    cudaEvent_t ev_fork, ev_read, ev_done;
 };
 
 namespace {
+
+constexpr uint64_t kAccBytes = 64ull << 20;
+
+// aux waits until `s` reaches this point
+b3g_status fork_aux(b3g_hasher *h, cudaStream_t s) {
+    cudaError_t e = cudaEventRecord(h->ev_fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->aux, h->ev_fork, 0);
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "fork to the side stream");
+}
+
+// the side stream's reads of segments and of acc, so far, end here
+b3g_status mark_read(b3g_hasher *h) {
+    cudaError_t e = cudaEventRecord(h->ev_read, h->aux);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    h->read_pending = true;
+    return B3G_OK;
+}
+
+// `s` waits for those reads: afterwards the segment may be reused and acc rewritten
+b3g_status join_reads(b3g_hasher *h, cudaStream_t s) {
+    if (!h->read_pending) return B3G_OK;
+    cudaError_t e = cudaStreamWaitEvent(s, h->ev_read, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+    h->read_pending = false;
+    return B3G_OK;
+}
+
+// `s` waits for everything queued on the side stream
+b3g_status join_all(b3g_hasher *h, cudaStream_t s) {
+    cudaError_t e = cudaEventRecord(h->ev_done, h->aux);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_done, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "join the side stream");
+    h->read_pending = false;
+    return B3G_OK;
+}
+
+b3g_status streams_init(b3g_hasher *h, bool own) {
+    h->own_streams = own;
+    h->read_pending = false;
+    h->aux = nullptr;
+    h->ev_fork = h->ev_read = h->ev_done = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (own) {
+        int least = 0, greatest = 0;
+        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->aux, cudaStreamNonBlocking, greatest);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithPriority");
+    } else {
+        b3g_status st = cached_stream(1, &h->aux);
+        if (st != B3G_OK) return st;
+    }
+    cudaEvent_t *evs[3] = {&h->ev_fork, &h->ev_read, &h->ev_done};
+    for (cudaEvent_t *ev : evs)
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "cudaEventCreateWithFlags");
+}
+
+void streams_release(b3g_hasher *h) {
+    if (h->aux) cudaStreamSynchronize(h->aux);
+    cudaEvent_t evs[3] = {h->ev_fork, h->ev_read, h->ev_done};
+    for (cudaEvent_t ev : evs)
+        if (ev) cudaEventDestroy(ev);
+    if (h->own_streams && h->aux) cudaStreamDestroy(h->aux);
+    h->aux = nullptr;
+    h->ev_fork = h->ev_read = h->ev_done = nullptr;
+}
 
 // The aligned power-of-two pieces of the chunk run [pos, pos + n): at every position
 // the largest power of two that divides the position and fits; a piece that starts at
@@ -424,18 +513,21 @@ std::vector<Piece> decompose(uint64_t pos, uint64_t n) {
     return pieces;
 }
 
-// One piece at a time: a subtree launch per piece and a merge launch before each push.
+// One piece at a time, all on the side stream: a subtree launch per piece and a merge
+// launch before each push.
 b3g_status push_pieces_one_by_one(b3g_hasher *h, const uint8_t *p, const std::vector<Piece> &pieces,
                                   cudaStream_t s) {
+    b3g_status st = fork_aux(h, s);
+    if (st != B3G_OK) return st;
+    const cudaStream_t x = h->aux;
     uint64_t biggest = 0;
     for (const Piece &pc : pieces) biggest = pc.size > biggest ? pc.size : biggest;
     const size_t ws_bytes = blake3_workspace_size(biggest * kChunkBytes);
     uint8_t *ws = nullptr;
     if (ws_bytes) {
-        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), ws_bytes, s);
+        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), ws_bytes, x);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
     }
-    b3g_status st = B3G_OK;
     const uint64_t base = h->pushed;
     for (const Piece &pc : pieces) {
         const uint32_t target = popcount64(pc.pos);
@@ -443,7 +535,7 @@ b3g_status push_pieces_one_by_one(b3g_hasher *h, const uint8_t *p, const std::ve
             RecordArgs ra = record_args(h->state, h->kw, kRecMerge);
             ra.depth = h->depth;
             ra.target = target;
-            st = launch_record(ra, s);
+            st = launch_record(ra, x);
             if (st != B3G_OK) break;
             h->depth = target;
         }
@@ -452,26 +544,47 @@ b3g_status push_pieces_one_by_one(b3g_hasher *h, const uint8_t *p, const std::ve
             break;
         }
         st = hash_range_ws(p + (pc.pos - base) * kChunkBytes, pc.size * kChunkBytes, pc.pos, h->key, false,
-                           h->state + 32ull * h->depth, ws, s);
+                           h->state + 32ull * h->depth, ws, x);
         if (st != B3G_OK) break;
         h->depth += 1;
         h->pushed = pc.pos + pc.size;
     }
     if (ws) {
-        cudaError_t e = cudaFreeAsync(ws, s);
+        cudaError_t e = cudaFreeAsync(ws, x);
         if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
+    }
+    const b3g_status rs = mark_read(h);
+    return st != B3G_OK ? st : rs;
+}
+
+// One full chunk at `p`: a record launch on the side stream merges and pushes its CV.
+b3g_status push_one(b3g_hasher *h, const uint8_t *p, cudaStream_t s) {
+    b3g_status st = fork_aux(h, s);
+    if (st != B3G_OK) return st;
+    RecordArgs ra = record_args(h->state, h->kw, kRecPush);
+    ra.in = p;
+    ra.depth = h->depth;
+    ra.target = popcount64(h->pushed);
+    ra.pushed = h->pushed;
+    st = launch_record(ra, h->aux);
+    if (st == B3G_OK) st = mark_read(h);
+    if (st == B3G_OK) {
+        h->depth = ra.target + 1;
+        h->pushed += 1;
     }
     return st;
 }
 
 // Push the chunks [h->pushed, h->pushed + nchunks) that start at `p`.  Batched: the
 // pieces shorter than a CTA subtree (only at the two ends of the run) go through one
-// launch of pieces_kernel; the longer pieces are contiguous and aligned to a CTA
-// subtree, so one leaf launch over their union yields their tile CVs, and one launch of
-// ranges_reduce_kernel (plus the ordinary reduction for pieces of more than 1024
-// tiles) turns those into piece roots; one record_kernel launch then does every merge
-// and push in order.
+// launch of pieces_kernel on the side stream; the longer pieces are contiguous and
+// aligned to a CTA subtree, so one leaf launch over their union (on `s`) yields their
+// tile CVs, and one launch of ranges_reduce_kernel (plus the ordinary reduction for
+// pieces of more than 1024 tiles) turns those into piece roots; one record_kernel
+// launch then does every merge and push in order.  Everything after the leaf launch
+// runs on the side stream.
 b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStream_t s) {
+    if (nchunks == 1) return push_one(h, p, s);
     const std::vector<Piece> pieces = decompose(h->pushed, nchunks);
     const uint64_t tile = 1ull << kDefaultLeavesLog2;
     const uint64_t base = h->pushed;
@@ -507,7 +620,12 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
     uint8_t *roots = scratch;
     uint8_t *tile_cvs = scratch + roots_bytes;
     uint8_t *huge = tile_cvs + tiles_bytes;
-    b3g_status st = B3G_OK;
+    const cudaStream_t x = h->aux;
+    b3g_status st = fork_aux(h, s);  // the side stream sees the segment and the scratch
+    if (st != B3G_OK) {
+        cudaFreeAsync(scratch, s);
+        return st;
+    }
 
     if (!small.empty()) {
         PiecesArgs pa;
@@ -522,9 +640,9 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
             pa.nchunks[i] = static_cast<uint32_t>(pc.size);
             pa.slot[i] = static_cast<uint32_t>(small[i]);
         }
-        pieces_kernel<<<static_cast<unsigned>(small.size()), 64, 0, s>>>(pa);
+        pieces_kernel<<<static_cast<unsigned>(small.size()), 64, 0, x>>>(pa);
         e = cudaGetLastError();
-        if (e != cudaSuccess) st = cuda_fail(e, "pieces_kernel launch");
+        st = e == cudaSuccess ? mark_read(h) : cuda_fail(e, "pieces_kernel launch");
     }
     if (st == B3G_OK && !big.empty()) {
         uint32_t *status = nullptr;
@@ -543,6 +661,7 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
             std::memcpy(a.key, h->kw, sizeof a.key);
             st = launch_leaf(a, kDefaultLeavesLog2, false, s);
         }
+        if (st == B3G_OK) st = fork_aux(h, s);  // the tile CVs are ready
         RangesArgs ra;
         std::memset(&ra, 0, sizeof ra);
         ra.in = tile_cvs;
@@ -554,7 +673,7 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
             const uint64_t t0 = (pieces[j].pos - A) / tile, t = pieces[j].size / tile;
             if (t > 1024) {  // a very large piece: the ordinary multi-level reduction
                 st = blake3_keyed_reduce_cvs(tile_cvs + 32 * t0, t, h->key, 0, 10, roots + 32 * j, huge, huge_ws,
-                                             reinterpret_cast<b3g_stream_t>(s));
+                                             reinterpret_cast<b3g_stream_t>(x));
                 continue;
             }
             ra.start[nr] = static_cast<uint32_t>(t0);
@@ -565,7 +684,7 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
         }
         if (st == B3G_OK && nr) {
             const unsigned threads = widest / 2 < 32 ? 32 : widest / 2;
-            ranges_reduce_kernel<<<nr, threads, 0, s>>>(ra);
+            ranges_reduce_kernel<<<nr, threads, 0, x>>>(ra);
             e = cudaGetLastError();
             if (e != cudaSuccess) st = cuda_fail(e, "ranges_reduce_kernel launch");
         }
@@ -581,15 +700,52 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
             const uint32_t target = popcount64(pieces[j].pos);
             d = (d > target ? target : d) + 1;
         }
-        st = launch_record(rec, s);
+        st = launch_record(rec, x);
         if (st == B3G_OK) {
             h->depth = d;
             h->pushed = base + nchunks;
         }
     }
-    e = cudaFreeAsync(scratch, s);
+    e = cudaFreeAsync(scratch, x);
     if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
     return st;
+}
+
+// Appends len bytes at p to acc (a copy on `s`).
+b3g_status append_acc(b3g_hasher *h, const uint8_t *p, uint64_t len, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyAsync(h->acc + h->acc_len, p, len, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+    h->acc_len += len;
+    return B3G_OK;
+}
+
+// Moves acc to an own kAccBytes buffer.  If the allocation fails the hasher keeps the
+// 1024-byte buffer (and stops trying).
+b3g_status grow_acc(b3g_hasher *h, cudaStream_t s) {
+    uint8_t *bigger = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&bigger), kAccBytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        h->may_grow = false;
+        return B3G_OK;
+    }
+    if (h->acc_len) {
+        e = cudaMemcpyAsync(bigger, h->acc, h->acc_len, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) {
+            cudaFree(bigger);
+            return cuda_fail(e, "cudaMemcpyAsync");
+        }
+    }
+    h->acc = bigger;
+    h->acc_cap = kAccBytes;
+    h->may_grow = false;
+    return B3G_OK;
+}
+
+void hasher_clear(b3g_hasher *h) {
+    h->count = h->pushed = 0;
+    h->depth = 0;
+    h->acc_len = 0;
 }
 
 }  // namespace
@@ -643,13 +799,23 @@ b3g_status blake3_hasher_new(const uint8_t key[32], b3g_hasher **out) {
     if (!h) return B3G_ERR_ARG;
     std::memcpy(h->key, key, 32);
     key_words(key, h->kw);
-    h->count = h->pushed = 0;
-    h->depth = h->buf_len = 0;
+    hasher_clear(h);
+    h->state = nullptr;
     cudaError_t e = cudaGetDevice(&h->device);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void **>(&h->state), kStateBytes);
     if (e != cudaSuccess) {
         delete h;
         return cuda_fail(e, "blake3_hasher_new");
+    }
+    h->acc = h->state + kBufOff;
+    h->acc_cap = kChunkBytes;
+    h->may_grow = true;
+    const b3g_status st = streams_init(h, true);
+    if (st != B3G_OK) {
+        streams_release(h);
+        cudaFree(h->state);
+        delete h;
+        return st;
     }
     *out = h;
     return B3G_OK;
@@ -659,6 +825,8 @@ void blake3_hasher_free(b3g_hasher *h) {
     if (!h) return;
     int prev = -1;
     if (cudaGetDevice(&prev) == cudaSuccess && prev != h->device) cudaSetDevice(h->device);
+    streams_release(h);
+    if (h->acc != h->state + kBufOff) cudaFree(h->acc);
     cudaFree(h->state);
     if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
     delete h;
@@ -666,8 +834,7 @@ void blake3_hasher_free(b3g_hasher *h) {
 
 b3g_status blake3_hasher_reset(b3g_hasher *h) {
     if (!h) return B3G_ERR_NULL;
-    h->count = h->pushed = 0;
-    h->depth = h->buf_len = 0;
+    hasher_clear(h);
     return B3G_OK;
 }
 
@@ -680,52 +847,55 @@ b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b
     if (st != B3G_OK) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint8_t *p = static_cast<const uint8_t *>(d_in);
-    uint8_t *buf = h->state + kBufOff;
-    cudaError_t e;
-    // at most one chunk in total: keep the bytes, it may be the whole input
-    if (h->count + len <= kChunkBytes) {
-        e = cudaMemcpyAsync(buf + h->buf_len, p, len, cudaMemcpyDeviceToDevice, s);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
-        h->buf_len += static_cast<uint32_t>(len);
-        h->count += len;
-        return B3G_OK;
+    // under stream capture: no allocation outside the stream, and the side stream
+    // rejoins completely, so that the captured graph is closed
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
+    if (h->acc_len + len > h->acc_cap && h->may_grow && !capturing && len < kAccBytes) {
+        st = grow_acc(h, s);
+        if (st != B3G_OK) return st;
     }
+    // fits: keep the bytes (while the input is at most one chunk this is required, the
+    // chunk may turn out to be the whole input and then needs ROOT)
+    if (h->acc_len + len <= h->acc_cap) {
+        st = append_acc(h, p, len, s);
+        if (st == B3G_OK) h->count += len;
+        return st;
+    }
+    // more than acc holds, so more input follows every chunk in acc: complete its last
+    // chunk, push all of acc, then push the segment's whole chunks if they do not fit
+    // in acc either, and keep the rest
     uint64_t rest = len;
-    // complete the buffered chunk, and push it once it is full
-    if (h->buf_len > 0) {
-        const uint64_t fill = kChunkBytes - h->buf_len < rest ? kChunkBytes - h->buf_len : rest;
-        if (fill) {
-            e = cudaMemcpyAsync(buf + h->buf_len, p, fill, cudaMemcpyDeviceToDevice, s);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
-        }
-        h->buf_len += static_cast<uint32_t>(fill);
+    const uint64_t fill_to = (kChunkBytes - h->acc_len % kChunkBytes) % kChunkBytes;
+    const uint64_t fill = fill_to < rest ? fill_to : rest;
+    if (fill) {
+        st = append_acc(h, p, fill, s);
+        if (st != B3G_OK) return st;
         p += fill;
         rest -= fill;
-        h->count += fill;
-        if (h->buf_len < kChunkBytes) return B3G_OK;
-        RecordArgs ra = record_args(h->state, h->kw, kRecPush);
-        ra.depth = h->depth;
-        ra.target = popcount64(h->pushed);
-        ra.pushed = h->pushed;
-        st = launch_record(ra, s);
-        if (st != B3G_OK) return st;
-        h->depth = ra.target + 1;
-        h->pushed += 1;
-        h->buf_len = 0;
     }
-    // whole chunks, then the unfinished tail into the buffer
-    const uint64_t full = rest / kChunkBytes;
-    if (full) {
+    if (h->acc_len) {
+        st = push_run(h, h->acc, h->acc_len / kChunkBytes, s);
+        if (st != B3G_OK) return st;
+        h->acc_len = 0;
+    }
+    if (rest > h->acc_cap) {
+        const uint64_t full = rest / kChunkBytes;
         st = push_run(h, p, full, s);
         if (st != B3G_OK) return st;
+        p += full * kChunkBytes;
+        rest -= full * kChunkBytes;
     }
-    const uint64_t tail = rest - full * kChunkBytes;
-    if (tail) {
-        e = cudaMemcpyAsync(buf, p + full * kChunkBytes, tail, cudaMemcpyDeviceToDevice, s);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+    // the side stream has read acc and the segment before `s` goes on
+    st = capturing ? join_all(h, s) : join_reads(h, s);
+    if (st != B3G_OK) return st;
+    if (rest) {
+        st = append_acc(h, p, rest, s);
+        if (st != B3G_OK) return st;
     }
-    h->buf_len = static_cast<uint32_t>(tail);
-    h->count += rest;
+    h->count += len;
     return B3G_OK;
 }
 
@@ -734,10 +904,12 @@ b3g_status blake3_keyed_hash_host(const void *h_in, uint64_t len, const uint8_t 
     if (!key || !out32 || (!h_in && len > 0)) return B3G_ERR_NULL;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaStream_t cs = nullptr;
-    b3g_status st = copy_stream(&cs);
+    b3g_status st = cached_stream(0, &cs);
     if (st != B3G_OK) return st;
     constexpr size_t kSlotAlign = 1u << 20;
     constexpr size_t kHead = (kStateBytes + 255) & ~size_t(255);  // hasher state + digest
+    if (d_staging && (reinterpret_cast<uintptr_t>(d_staging) & 255u)) return B3G_ERR_ALIGN;
+    if (d_staging && staging_bytes < kHead + 2 * kSlotAlign) return B3G_ERR_WORKSPACE;
     bool own = false;
     if (!d_staging) {
         staging_bytes = kHead + 2 * (64u << 20);
@@ -745,27 +917,33 @@ b3g_status blake3_keyed_hash_host(const void *h_in, uint64_t len, const uint8_t 
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
         own = true;
     }
-    if (reinterpret_cast<uintptr_t>(d_staging) & 255u) return B3G_ERR_ALIGN;
-    if (staging_bytes < kHead + 2 * kSlotAlign) return B3G_ERR_WORKSPACE;
     const size_t slot = ((staging_bytes - kHead) / 2) & ~(kSlotAlign - 1);
     uint8_t *base = static_cast<uint8_t *>(d_staging);
     uint8_t *slots[2] = {base + kHead, base + kHead + slot};
 
+    // a hasher whose state lives in the staging area; slot-sized segments bypass acc
     b3g_hasher h;
     std::memcpy(h.key, key, 32);
     key_words(key, h.kw);
+    hasher_clear(&h);
+    h.own_streams = h.read_pending = false;
+    h.aux = nullptr;
+    h.ev_fork = h.ev_read = h.ev_done = nullptr;
     h.state = base;
-    h.count = h.pushed = 0;
-    h.depth = h.buf_len = 0;
+    h.acc = base + kBufOff;
+    h.acc_cap = kChunkBytes;
+    h.may_grow = false;
     cudaError_t e = cudaGetDevice(&h.device);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (e != cudaSuccess) st = cuda_fail(e, "cudaGetDevice");
+    if (st == B3G_OK) st = streams_init(&h, false);
 
     cudaEvent_t ev[5] = {};
-    for (int i = 0; i < 5 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    for (int i = 0; i < 5 && st == B3G_OK && e == cudaSuccess; ++i)
+        e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
     cudaEvent_t start = ev[0], copied[2] = {ev[1], ev[2]}, consumed[2] = {ev[3], ev[4]};
-    if (e == cudaSuccess) e = cudaEventRecord(start, s);  // staging is free once the stream reaches here
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, start, 0);
-    if (e != cudaSuccess) st = cuda_fail(e, "event set-up");
+    if (st == B3G_OK && e == cudaSuccess) e = cudaEventRecord(start, s);  // staging is free from here on
+    if (st == B3G_OK && e == cudaSuccess) e = cudaStreamWaitEvent(cs, start, 0);
+    if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "event set-up");
     const uint8_t *src = static_cast<const uint8_t *>(h_in);
     uint64_t off = 0;
     for (uint64_t i = 0; st == B3G_OK && off < len; ++i) {
@@ -787,6 +965,7 @@ b3g_status blake3_keyed_hash_host(const void *h_in, uint64_t len, const uint8_t 
     if (st == B3G_OK) st = blake3_hasher_finalize(&h, d_digest, 32, stream);
     if (st == B3G_OK && (e = cudaMemcpyAsync(out32, d_digest, 32, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
         st = cuda_fail(e, "cudaMemcpyAsync(digest)");
+    if (h.aux && h.ev_done) join_all(&h, s);  // also after an error: nothing on the side stream outlives the staging
     if (own) {
         e = cudaFreeAsync(d_staging, s);
         if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
@@ -795,28 +974,57 @@ b3g_status blake3_keyed_hash_host(const void *h_in, uint64_t len, const uint8_t 
     if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaStreamSynchronize");
     for (cudaEvent_t x : ev)
         if (x) cudaEventDestroy(x);
+    streams_release(&h);
     return st;
 }
 
-b3g_status blake3_hasher_finalize(const b3g_hasher *h, uint8_t *d_out, uint64_t out_len, b3g_stream_t stream) {
-    if (!h || (!d_out && out_len > 0)) return B3G_ERR_NULL;
-    b3g_status st = check_device(h->device);
+b3g_status blake3_hasher_finalize(const b3g_hasher *hc, uint8_t *d_out, uint64_t out_len, b3g_stream_t stream) {
+    if (!hc || (!d_out && out_len > 0)) return B3G_ERR_NULL;
+    b3g_status st = check_device(hc->device);
     if (st != B3G_OK) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    RecordArgs ra = record_args(h->state, h->kw, kRecFinalize);
-    if (h->count <= kChunkBytes) {
-        ra.mode = kRecChunk;
-        ra.in = h->state + kBufOff;
-        ra.len = static_cast<uint32_t>(h->count);
-        ra.pushed = 0;
-    } else {
-        ra.depth = h->depth;
-        ra.pushed = h->pushed;
-        ra.len = h->buf_len;
-    }
-    st = launch_record(ra, s);
+    // a working copy: chunks still in acc are pushed onto a scratch copy of the stack,
+    // so the hasher itself is unchanged
+    b3g_hasher t = *hc;
+    st = join_all(&t, s);
     if (st != B3G_OK) return st;
-    return launch_xof(reinterpret_cast<const uint32_t *>(h->state + kRecordOff), d_out, out_len, s);
+    if (t.count <= kChunkBytes) {
+        RecordArgs ra = record_args(t.state, t.kw, kRecChunk);
+        ra.in = t.acc;
+        ra.len = static_cast<uint32_t>(t.count);
+        st = launch_record(ra, s);
+        if (st != B3G_OK) return st;
+        return launch_xof(reinterpret_cast<const uint32_t *>(t.state + kRecordOff), d_out, out_len, s);
+    }
+    // every chunk of acc but the last is pushed; the last (1..1024 bytes) is finished by
+    // the record launch
+    const uint64_t k = t.acc_len ? (t.acc_len - 1) / kChunkBytes : 0;
+    uint8_t *scratch = nullptr;
+    cudaError_t e;
+    if (k) {
+        e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), kStateBytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
+        if (t.depth) e = cudaMemcpyAsync(scratch, t.state, 32ull * t.depth, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) st = cuda_fail(e, "cudaMemcpyAsync");
+        t.state = scratch;
+        if (st == B3G_OK) st = push_run(&t, t.acc, k, s);
+        const b3g_status js = join_all(&t, s);
+        if (st == B3G_OK) st = js;
+    }
+    if (st == B3G_OK) {
+        RecordArgs ra = record_args(t.state, t.kw, kRecFinalize);
+        ra.in = t.acc + k * kChunkBytes;
+        ra.len = static_cast<uint32_t>(t.acc_len - k * kChunkBytes);
+        ra.depth = t.depth;
+        ra.pushed = t.pushed;
+        st = launch_record(ra, s);
+    }
+    if (st == B3G_OK) st = launch_xof(reinterpret_cast<const uint32_t *>(t.state + kRecordOff), d_out, out_len, s);
+    if (scratch) {
+        e = cudaFreeAsync(scratch, s);
+        if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
+    }
+    return st;
 }
 
 }  // extern "C"

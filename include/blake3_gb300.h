@@ -216,20 +216,28 @@ b3g_status blake3_keyed_hash_xof(const void *d_in, uint64_t len, const uint8_t k
 /*
  * Streaming hasher: the digest of input that arrives as successive device segments of
  * any length, equal to the digest of their concatenation.  The hasher is a host object
- * that owns about 3 KiB of device memory on the device current at creation; every call
- * must be made with that device current (else B3G_ERR_ARG).  Calls are asynchronous on
- * the stream passed; a hasher must be used from one stream at a time (calls in stream
- * order), and a segment may be reused once the update's work on that stream is done.
- * Whole runs of chunks inside a segment go through the same leaf and reduction
- * kernels as blake3_keyed_hash; chaining values are merged only once more input is
- * known to follow (page section "BLAKE3": the tree rules).
+ * that owns, on the device current at creation, about 3 KiB of device memory, a side
+ * stream of the highest priority and three events; the first update shorter than
+ * 64 MiB that does not fit in what is buffered adds a 64 MiB accumulation buffer
+ * (cudaMalloc; if that fails the hasher goes on without it).  Every call must be made
+ * with that device current (else B3G_ERR_ARG).  Calls are asynchronous on the stream
+ * passed; a hasher must be used from one stream at a time (calls in stream order), and
+ * a segment may be reused once the update's work on that stream is done.  Segments
+ * are copied into the accumulation buffer while they fit and pushed in large batches;
+ * whole runs of chunks go through the same leaf and reduction kernels as
+ * blake3_keyed_hash, and the small launches after them run on the side stream, joined
+ * back to the caller's stream by events (fully, when the caller's stream is being
+ * captured into a graph).  Chaining values are merged only once more input is known to
+ * follow (page section "BLAKE3": the tree rules).
  */
 typedef struct b3g_hasher b3g_hasher;
 
-/* Creates a hasher for `key` (host pointer, copied).  Allocates with cudaMalloc. */
+/* Creates a hasher for `key` (host pointer, copied).  Allocates with cudaMalloc and
+ * creates its side stream and events. */
 b3g_status blake3_hasher_new(const uint8_t key[32], b3g_hasher **out);
 
-/* Frees the hasher and its device memory (cudaFree synchronises the device). */
+/* Frees the hasher, its device memory, stream and events (waits for its side stream;
+ * cudaFree synchronises the device). */
 void blake3_hasher_free(b3g_hasher *h);
 
 /* Forgets all input (same key).  Host-side only. */

@@ -127,3 +127,83 @@ def test_hash_from_host_rejects_small_staging():
     staging = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
     with pytest.raises(binding.B3GError):
         binding.blake3_keyed_hash_host(host, KEY, staging)
+
+
+def test_hasher_very_large_piece():
+    """A piece of more than 1024 CTA subtrees inside one update (chunks 2^18 .. 2^19):
+    the multi-level reduction branch of the batched push."""
+    total = 2048 + (600 << 20) + 5
+    host = workloads.uniform_bytes(600, total)
+    d = host.cuda()
+    h = binding.Hasher(KEY)
+    h.update(d[:2048])
+    h.update(d[2048:])
+    got = bytes(h.finalize().cpu().numpy())
+    assert got == bytes(binding.blake3_keyed_hash(d, KEY).cpu().numpy())
+    assert got == oracle.keyed_hash(host, KEY)
+
+
+def test_hasher_many_small_segments():
+    """About 140 MiB in segments of 1 B .. 3 MB: they collect in the 64 MiB accumulation
+    buffer, which is pushed twice; digests taken in between push the buffered chunks
+    onto a copy of the stack only."""
+    total = (140 << 20) + 12345
+    host = workloads.uniform_bytes(1400, total)
+    d = host.cuda()
+    rng = np.random.default_rng(1400)
+    h = binding.Hasher(KEY)
+    checks = {30 << 20, 90 << 20}
+    a = 0
+    while a < total:
+        n = int(min(total - a, rng.integers(1, 3_000_000)))
+        if rng.random() < 0.1:
+            n = int(min(total - a, rng.integers(1, 2048)))
+        h.update(d[a:a + n])
+        a += n
+        hit = [c for c in checks if c <= a]
+        for c in hit:
+            checks.discard(c)
+            got = bytes(h.finalize().cpu().numpy())
+            assert got == bytes(binding.blake3_keyed_hash(d[:a], KEY).cpu().numpy()), a
+    assert h.count == total
+    got = bytes(h.finalize().cpu().numpy())
+    assert got == oracle.keyed_hash(host, KEY)
+    assert bytes(h.finalize(100).cpu().numpy()) == oracle.keyed_hash_xof(host, KEY, 100)
+
+
+def test_hasher_buffer_growth_and_mixed_sizes():
+    """Small, larger-than-buffer and exactly-buffer-sized segments in turn; every prefix
+    digest equals the one-shot digest of that prefix."""
+    sizes = [5, 3000, (70 << 20) + 13, 1 << 20, 64 << 20, 100, 1024, 2047, (64 << 20) - 1, 1, 9 << 20]
+    total = sum(sizes)
+    host = workloads.uniform_bytes(1401, total)
+    d = host.cuda()
+    h = binding.Hasher(KEY)
+    a = 0
+    for n in sizes:
+        h.update(d[a:a + n])
+        a += n
+        got = bytes(h.finalize().cpu().numpy())
+        assert got == bytes(binding.blake3_keyed_hash(d[:a], KEY).cpu().numpy()), (n, a)
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
+    h.reset()
+    h.update(d[:500])
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host[:500], KEY)
+    h.update(d[500:2048])
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host[:2048], KEY)
+
+
+@pytest.mark.parametrize("sizes", [[4096, 8192], [1024, 1024], [2048], [1024, 1], [1, 1023, 1024, 1024],
+                                   [5000, 1 << 20, 3 << 20]])
+def test_hasher_finalize_buffered_whole_chunks(sizes):
+    """The buffer holds only whole chunks (or one chunk and a byte) at finalize."""
+    total = sum(sizes)
+    host = workloads.uniform_bytes(1402 + total, total)
+    d = host.cuda()
+    h = binding.Hasher(KEY)
+    a = 0
+    for n in sizes:
+        h.update(d[a:a + n])
+        a += n
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
+    assert bytes(h.finalize(96).cpu().numpy()) == oracle.keyed_hash_xof(host, KEY, 96)
