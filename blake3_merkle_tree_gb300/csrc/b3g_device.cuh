@@ -89,30 +89,54 @@ __device__ __forceinline__ uint32_t add2(uint32_t c, uint32_t d) {
 #endif
 }
 
+// Rotations on the FMA pipe.  x * 2^k as a 64-bit product holds x << k in its low
+// word and x >> (32 - k) in its high word; the two share no bit, so their sum is the
+// rotation left by k (right by 32 - k): one multiply (low word) and one multiply-add
+// (high word plus the low word).  The multiplier comes from constant memory, so the
+// compiler keeps the multiplies instead of turning them into shifts.  Bit j of
+// B3G_ROT_FMA (G number j of a round: 0-3 columns, 4-7 diagonals) moves that G's
+// rotation by 7 to the FMA pipe, bit 8 + j its rotation by 12; 0 keeps every rotation
+// on the ALU pipe.
+#ifndef B3G_ROT_FMA
+#define B3G_ROT_FMA 0
+#endif
+
+static __constant__ uint32_t c_pow25 = 1u << 25;  // rotation right by 7
+static __constant__ uint32_t c_pow20 = 1u << 20;  // rotation right by 12
+
+__device__ __forceinline__ uint32_t rotr_fma(uint32_t x, uint32_t pow) {
+    uint32_t lo, r;
+    asm("mul.lo.u32 %0, %1, %2;" : "=r"(lo) : "r"(x), "r"(pow));
+    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(pow), "r"(lo));
+    return r;
+}
+
+template <int J>
 __device__ __forceinline__ void g(uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d, uint32_t x,
                                   uint32_t y) {
+    constexpr bool kFma7 = (B3G_ROT_FMA >> J) & 1, kFma12 = (B3G_ROT_FMA >> (8 + J)) & 1;
     a = add3(a, b, x);
     d = rotr16(d ^ a);
     c = add2(c, d);
-    b = rotr12(b ^ c);
+    b = kFma12 ? rotr_fma(b ^ c, c_pow20) : rotr12(b ^ c);
     a = add3(a, b, y);
     d = rotr8(d ^ a);
     c = add2(c, d);
-    b = rotr7(b ^ c);
+    b = kFma7 ? rotr_fma(b ^ c, c_pow25) : rotr7(b ^ c);
 }
 
 template <int R>
 __device__ __forceinline__ void round_fn(uint32_t v[16], const uint32_t m[16]) {
     // columns
-    g(v[0], v[4], v[8], v[12], m[msg_index(R, 0)], m[msg_index(R, 1)]);
-    g(v[1], v[5], v[9], v[13], m[msg_index(R, 2)], m[msg_index(R, 3)]);
-    g(v[2], v[6], v[10], v[14], m[msg_index(R, 4)], m[msg_index(R, 5)]);
-    g(v[3], v[7], v[11], v[15], m[msg_index(R, 6)], m[msg_index(R, 7)]);
+    g<0>(v[0], v[4], v[8], v[12], m[msg_index(R, 0)], m[msg_index(R, 1)]);
+    g<1>(v[1], v[5], v[9], v[13], m[msg_index(R, 2)], m[msg_index(R, 3)]);
+    g<2>(v[2], v[6], v[10], v[14], m[msg_index(R, 4)], m[msg_index(R, 5)]);
+    g<3>(v[3], v[7], v[11], v[15], m[msg_index(R, 6)], m[msg_index(R, 7)]);
     // diagonals
-    g(v[0], v[5], v[10], v[15], m[msg_index(R, 8)], m[msg_index(R, 9)]);
-    g(v[1], v[6], v[11], v[12], m[msg_index(R, 10)], m[msg_index(R, 11)]);
-    g(v[2], v[7], v[8], v[13], m[msg_index(R, 12)], m[msg_index(R, 13)]);
-    g(v[3], v[4], v[9], v[14], m[msg_index(R, 14)], m[msg_index(R, 15)]);
+    g<4>(v[0], v[5], v[10], v[15], m[msg_index(R, 8)], m[msg_index(R, 9)]);
+    g<5>(v[1], v[6], v[11], v[12], m[msg_index(R, 10)], m[msg_index(R, 11)]);
+    g<6>(v[2], v[7], v[8], v[13], m[msg_index(R, 12)], m[msg_index(R, 13)]);
+    g<7>(v[3], v[4], v[9], v[14], m[msg_index(R, 14)], m[msg_index(R, 15)]);
 }
 
 // One compression; cv (8 words) is replaced by the first 8 output words.

@@ -18,9 +18,15 @@
 //   - Persistent CTAs: the grid is sized to the resident capacity and each CTA walks
 //     tiles blockIdx.x, blockIdx.x + gridDim.x, ...; the stage ring keeps running
 //     across tiles, so the producer loads the next tile during the subtree phase.
-//   - One producer warp (one elected lane) instead of 128 producer threads; the
-//     consumers release a stage per warp (one arrive per warp on the "empty"
-//     barrier) instead of a consumer-wide barrier.
+//   - No producer threads: each consumer warp feeds itself.  Its lane 0 keeps a few
+//     bulk tensor copies of the warp's own 32 chunk rows in flight in a private
+//     ring and refills a stage as soon as the warp has read it, so no warp waits
+//     for another warp's progress (the page uses 128 producer threads and a
+//     consumer-wide barrier per stage).
+//   - One reducer warp per CTA turns the consumers' chunk CVs into the tile CV,
+//     taking them through two node buffers so that the consumers go on with the
+//     next tile at once; the top levels of several full tiles are reduced together
+//     so that those levels keep whole warps busy.
 //   - The box height is at most 256 rows (the TMA limit), so one tensor map and one
 //     pipeline cover every tile size up to 256 chunks; no dual pipeline is needed.
 //   - The partial last chunk is not padded inside the stage: rows past the last full
@@ -52,6 +58,20 @@
 #define B3G_LEAF_BOUNDS(threads) __launch_bounds__(threads, B3G_MIN_BLOCKS)
 #else
 #define B3G_LEAF_BOUNDS(threads) __launch_bounds__(threads)
+#endif
+// Full tiles whose top tree levels the reducer warp runs together (0: every tile on
+// its own), and whether the reducer's tree level is a called function (1) or inlined
+// at each use (0).
+#ifndef B3G_TOP_BATCH
+#define B3G_TOP_BATCH 8
+#endif
+#ifndef B3G_PAIR_NOINLINE
+#define B3G_PAIR_NOINLINE 0
+#endif
+#if B3G_PAIR_NOINLINE
+#define B3G_PAIR_ATTR __noinline__
+#else
+#define B3G_PAIR_ATTR __forceinline__
 #endif
 
 namespace b3g {
@@ -92,11 +112,20 @@ struct TmaCfg {
     static constexpr uint32_t kNodeBytes = C * 32;            // one node buffer
     static constexpr uint32_t kScratch1Bytes = (C / 2) * 32;  // odd tree levels
     static constexpr uint32_t kScratch2Bytes = (C / 4) * 32;  // even tree levels
-    // layout: [align 1024][rings][2 node buffers][scratch 1][scratch 2][barriers]
+    // the top five levels (32 nodes -> 1) of kTopBatch full tiles are reduced
+    // together, in two ping-pong buffers of 32 and 16 nodes per tile.  Only for
+    // 128-chunk tiles: smaller tiles serve small inputs (about one tile per CTA), and
+    // with 256-chunk tiles the buffers would cost a resident CTA per SM.
+    static constexpr uint32_t kTopBatch = (CHUNK_CVS || C != 128) ? 0 : B3G_TOP_BATCH;
+    static constexpr uint32_t kTopABytes = kTopBatch * 32 * 32;
+    static constexpr uint32_t kTopBBytes = kTopBatch * 16 * 32;
+    // layout: [align 1024][rings][2 node buffers][scratch 1][scratch 2][top A][top B][barriers]
     static constexpr uint32_t kOffNodes = kConsumerWarps * kRingBytes;
     static constexpr uint32_t kOffScratch1 = kOffNodes + 2 * kNodeBytes;
     static constexpr uint32_t kOffScratch2 = kOffScratch1 + kScratch1Bytes;
-    static constexpr uint32_t kOffBars = kOffScratch2 + kScratch2Bytes;
+    static constexpr uint32_t kOffTopA = kOffScratch2 + kScratch2Bytes;
+    static constexpr uint32_t kOffTopB = kOffTopA + kTopABytes;
+    static constexpr uint32_t kOffBars = kOffTopB + kTopBBytes;
     static constexpr uint32_t kNumBars = kConsumerWarps * S + 4;
     static constexpr size_t kSmemBytes = 1024 + size_t(kOffBars) + 8 * kNumBars;
     static_assert(S >= 2 && S <= kLoadsPerChunk, "stage count");
@@ -123,6 +152,19 @@ __device__ __noinline__ Words8 partial_chunk_cv(const uint8_t *in, uint64_t len,
                  last ? bytes - 64u * (nblocks - 1u) : 64u, flags);
     }
     return cv;
+}
+
+// One tree level in shared memory: node j of `dst` = parent(node 2j, node 2j+1 of
+// `src`) for j < half, the lanes of the calling warp striding over j.
+__device__ B3G_PAIR_ATTR void pair_level(uint32_t src, uint32_t dst, uint32_t half, Words8 key) {
+    const uint32_t lane = threadIdx.x & 31u;
+    for (uint32_t j = lane; j < half; j += 32) {
+        uint32_t l[8], r[8], p[8];
+        load_node(src, 2 * j, l);
+        load_node(src, 2 * j + 1, r);
+        parent(key.w, l, r, false, p);
+        store_node(dst, j, p);
+    }
 }
 
 // Fused final reduction (at most 32 tiles, one tile per CTA).  Called by a whole
@@ -191,6 +233,38 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
     if (warp == Cfg::kReducerWarp) {
         // -------------------------------- reducer --------------------------------
         if constexpr (!CHUNK_CVS) {
+            const uint32_t topA = rings0 + Cfg::kOffTopA;
+            const uint32_t topB = rings0 + Cfg::kOffTopB;
+            Words8 key8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) key8.w[i] = key[i];
+            // Full tiles are reduced down to 32 nodes each, which wait side by side in
+            // top A; every kTopBatch tiles the top levels of all of them run as one
+            // array (pairing never mixes two tiles: each holds a power-of-two count),
+            // so those levels keep whole warps busy instead of 16, 8, 4, 2 and 1 lanes.
+            uint32_t pending = 0;  // tiles waiting in top A
+            uint64_t first = 0;    // the first of them (the others follow at gridDim.x)
+            auto flush = [&]() {
+                if (pending == 0) return;
+                uint32_t n = pending * 32u, src = topA, dst = topB;
+                while (n > pending) {
+                    pair_level(src, dst, n >> 1, key8);
+                    __syncwarp();
+                    const uint32_t t = src;
+                    src = dst;
+                    dst = t;
+                    n >>= 1;
+                }
+                if (lane < pending) {
+                    uint32_t x[8];
+                    load_node(src, lane, x);
+                    uint4 *o = reinterpret_cast<uint4 *>(a.out + (first + static_cast<uint64_t>(lane) * gridDim.x) * 32);
+                    o[0] = make_uint4(x[0], x[1], x[2], x[3]);
+                    o[1] = make_uint4(x[4], x[5], x[6], x[7]);
+                }
+                __syncwarp();
+                pending = 0;
+            };
             uint32_t k = 0;
             for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
                 const uint32_t b = k & 1u;
@@ -201,21 +275,40 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
                 }
                 const uint64_t rem = a.n_chunks - tile * C;
                 uint32_t cnt = rem < C ? static_cast<uint32_t>(rem) : static_cast<uint32_t>(C);
+                if (Cfg::kTopBatch > 0 && cnt == C && !a.ticket && !(a.root && a.n_tiles == 1)) {
+                    // a full tile: its levels down to 32 nodes, the last into top A
+                    const uint32_t slot = topA + pending * 1024u;
+                    uint32_t src = src0, level = 0;
+                    for (uint32_t n = C; n > 32; n >>= 1, ++level) {
+                        const uint32_t dst = n == 64 ? slot : ((level & 1u) ? scratch2 : scratch1);
+                        pair_level(src, dst, n >> 1, key8);
+                        __syncwarp();
+                        if (level == 0) mbar_arrive(cvempty0 + 8 * b);  // node buffer read
+                        src = dst;
+                    }
+                    if (level == 0) {  // 32 chunks per tile: the node buffer is the top level
+                        uint32_t x[8];
+                        load_node(src0, lane, x);
+                        __syncwarp();
+                        mbar_arrive(cvempty0 + 8 * b);
+                        store_node(slot, lane, x);
+                        __syncwarp();
+                    }
+                    if (pending == 0) first = tile;
+                    if (++pending == Cfg::kTopBatch) flush();
+                    continue;
+                }
+                // a partial tile, a single-tile root or the fused final reduction: on its own
+                flush();
                 uint32_t src = src0;
                 uint32_t level = 0;
-                // Levels with more than 32 nodes: pairs (2j, 2j+1) -> node j, lanes
-                // striding over j, ping-ponging between two scratch buffers; an odd
-                // last node moves up unchanged.
+                // Levels with more than 32 nodes: pairs (2j, 2j+1) -> node j,
+                // ping-ponging between two scratch buffers; an odd last node moves up
+                // unchanged.
                 while (cnt > 32) {
                     const uint32_t dst = (level & 1u) ? scratch2 : scratch1;
                     const uint32_t half = cnt >> 1;
-                    for (uint32_t j = lane; j < half; j += 32) {
-                        uint32_t l[8], r[8], p[8];
-                        load_node(src, 2 * j, l);
-                        load_node(src, 2 * j + 1, r);
-                        parent(key, l, r, false, p);
-                        store_node(dst, j, p);
-                    }
+                    pair_level(src, dst, half, key8);
                     if ((cnt & 1u) && lane == 0) {
                         uint32_t t[8];
                         load_node(src, cnt - 1, t);
@@ -239,6 +332,7 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
                 }
                 if (a.ticket) fused_final_reduce(a, key);
             }
+            flush();
         }
         return;
     }
@@ -457,7 +551,7 @@ constexpr int kMaxDevices = 64;
 #define B3G_TUNE_LOAD256 64
 #endif
 #ifndef B3G_TUNE_S128
-#define B3G_TUNE_S128 3
+#define B3G_TUNE_S128 2
 #endif
 #ifndef B3G_TUNE_LOAD128
 #define B3G_TUNE_LOAD128 64
@@ -603,9 +697,12 @@ const char *kernel_config() {
     static char buf[160];
     static std::once_flag once;
     std::call_once(once, [] {
-        std::snprintf(buf, sizeof buf, "leaf_tma_kernel<%d,%d,%d> unroll=%d min_blocks=%d g_form=%d",
+        std::snprintf(buf, sizeof buf,
+                      "leaf_tma_kernel<%d,%d,%d> unroll=%d min_blocks=%d g_form=%d top_batch=%d pair_noinline=%d "
+                      "rot_fma=0x%x",
                       1 << kDefaultLeavesLog2, Tuning<(1 << kDefaultLeavesLog2)>::S,
-                      Tuning<(1 << kDefaultLeavesLog2)>::LOAD, kCopyLoopUnroll, B3G_MIN_BLOCKS, B3G_G_FORM);
+                      Tuning<(1 << kDefaultLeavesLog2)>::LOAD, kCopyLoopUnroll, B3G_MIN_BLOCKS, B3G_G_FORM,
+                      B3G_TOP_BATCH, B3G_PAIR_NOINLINE, static_cast<unsigned>(B3G_ROT_FMA));
     });
     return buf;
 }
