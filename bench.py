@@ -24,7 +24,6 @@ import os
 import statistics
 import subprocess
 import sys
-import tempfile
 import time
 
 import torch
@@ -55,7 +54,7 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling during the timed region."""
+    """nvidia-smi clocks/throttle sampling during the timed region (read through a pipe)."""
 
     FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -64,18 +63,22 @@ class ClockSampler:
     def __init__(self, gpu_id: str):
         self.gpu = gpu_id
         self.proc = None
-        self.path = None
+        self.lines: list[str] = []
+        self.reader = None
 
     def __enter__(self):
-        fd, self.path = tempfile.mkstemp(prefix="b3g_clocks_", suffix=".csv")
-        os.close(fd)
+        import threading
+
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self.reader = threading.Thread(target=lambda: self.lines.extend(self.proc.stdout), daemon=True)
+        self.reader.start()
+        time.sleep(0.3)
         return self
 
     def __exit__(self, *exc):
@@ -86,23 +89,22 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            self.reader.join(timeout=5)
 
     def summary(self):
-        if self.proc is None or not self.path or not os.path.exists(self.path):
+        if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                if self.gpu and self.gpu.lower() not in parts[0].lower():
-                    continue
-                try:
-                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
-                except ValueError:
-                    continue
-        os.unlink(self.path)
+        for line in list(self.lines):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.gpu and self.gpu.lower() not in parts[0].lower():
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         loaded = [r for r in rows if r[2] > 0.5 * max(x[2] for x in rows)] or rows
@@ -125,6 +127,20 @@ def _traffic_per_launch(lib, nchunks):
         return None, "capture is of another kernel configuration"
     per_chunk = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) / rec["chunks"]
     return per_chunk * nchunks, f"ncu capture on {rec['workload']} scaled by chunks ({rec['chunks']} -> {nchunks})"
+
+
+def _max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over all ranks: a job takes as long as its slowest rank."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_gbs(bytes_per_rank: int, steps: int, total_ms: float, world: int) -> float:
+    """Whole-job GB/s: every rank hashes its own copy of the workload (weak scaling)."""
+    return world * bytes_per_rank * steps / (total_ms / 1e3) / 1e9
 
 
 def _dist():
@@ -258,12 +274,9 @@ def run_ours(args):
         torch.distributed.barrier()
     total_ms = starts[0].elapsed_time(end)
     leaf_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = _max_over_ranks(total_ms, world, "cuda")
     ms_per_step = total_ms / args.steps
-    value = world * n * args.steps / (total_ms / 1e3) / 1e9
+    value = _job_gbs(n, args.steps, total_ms, world)
 
     # roofline of the leaf kernel (integer issue bound)
     nchunks = max(1, -(-n // 1024))
