@@ -128,10 +128,9 @@ LeafArgs leaf_args(const void *d_in, uint64_t len, uint64_t chunk_offset, const 
     return a;
 }
 
-// Chunks per CTA subtree (log2) for an input of n chunks.  Large inputs use 256.
-// An input of at most 2^16 chunks (64 MiB) cannot fill the GPU with 256-chunk CTAs,
-// so the subtree shrinks (down to 32 chunks) until there are at least kSpreadTiles
-// CTAs: each chunk is a chain of 16 dependent compressions, so small inputs finish
+// Chunks per CTA subtree (log2) for an input of n chunks.  Large inputs use
+// 2^kDefaultLeavesLog2 (128).  For an input of at most 2^16 chunks (64 MiB) the
+// subtree shrinks (down to 32 chunks) until there are at least kSpreadTiles CTAs: each chunk is a chain of 16 dependent compressions, so small inputs finish
 // sooner with fewer warps per SM.  A function of n alone, so that the workspace size
 // is a function of the length alone.
 constexpr uint64_t kSmallInputChunks = 1ull << 16;

@@ -207,3 +207,25 @@ def test_hasher_finalize_buffered_whole_chunks(sizes):
         a += n
     assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
     assert bytes(h.finalize(96).cpu().numpy()) == oracle.keyed_hash_xof(host, KEY, 96)
+
+
+def test_hasher_updates_captured_in_a_cuda_graph():
+    """Updates captured into a CUDA graph and replayed once give the oracle digest: under
+    capture the side stream rejoins the capturing stream completely and the buffer does not
+    grow (no allocation outside the stream)."""
+    total = 3 * 1024 + (5 << 20) + 333
+    host = workloads.uniform_bytes(1500, total)
+    d = host.cuda()
+    binding.blake3_keyed_hash(d, KEY)  # first-use set-up (status word, occupancy) outside the capture
+    h = binding.Hasher(KEY)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    cuts = [0, 700, 3 * 1024 + 5, (2 << 20) + 77, total]
+    with torch.cuda.graph(g, stream=s):
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            h.update(d[a:b])
+    g.replay()
+    torch.cuda.synchronize()
+    assert h.count == total
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
