@@ -264,6 +264,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch.  A grid launched with programmatic stream
+// serialization may start before the grid ahead of it in the stream has finished;
+// grid_dependency_wait() returns once that grid has completed and its memory writes
+// are visible (at once if there is none).  launch_dependents() lets the grid behind
+// this one start early (its CTAs then wait in grid_dependency_wait()).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -73,6 +73,25 @@ b3g_status launch_wait_probe(uint64_t limit_ns, int *d_flag, cudaStream_t stream
 // Records a CUDA error for blake3_last_cuda_error() and returns B3G_ERR_CUDA.
 b3g_status cuda_fail(cudaError_t err, const char *what);
 
+// Launch with programmatic stream serialization: the grid may start while the grid
+// ahead of it in the stream is finishing.  Every kernel launched this way calls
+// grid_dependency_wait() before its first global-memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Device address of the current device's status word (looked up once per device).
 b3g_status device_status_word(uint32_t **out);
 

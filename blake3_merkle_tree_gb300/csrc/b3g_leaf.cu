@@ -216,7 +216,13 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
     const uint32_t warp = tid >> 5;
     const uint32_t lane = tid & 31u;
 
+    // launched early behind the previous kernel of the stream: no global-memory access
+    // before it has finished (it may still read this launch's output buffer)
+    grid_dependency_wait();
     if (tid == 0) {
+        // the reduction launched behind this kernel may start now: its CTAs take the
+        // places of finished CTAs and wait for this grid's results
+        launch_dependents();
         for (int i = 0; i < Cfg::kConsumerWarps * S; ++i) mbar_init(full0 + 8 * i, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(cvfull0 + 8 * b, C);
@@ -484,6 +490,8 @@ template <int C, bool CHUNK_CVS>
 __global__ void __launch_bounds__(C) leaf_direct_kernel(const LeafArgs a) {
     __shared__ __align__(128) uint8_t node_mem[C * 32];
     const uint32_t nodes = smem_u32(node_mem);
+    grid_dependency_wait();  // see leaf_tma_kernel
+    if (threadIdx.x == 0) launch_dependents();
     uint32_t key[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) key[i] = a.key[i];
@@ -667,8 +675,8 @@ b3g_status launch_tma(const LeafArgs &a, cudaStream_t stream, int dev, const Dev
     b3g_status st = kernel_blocks_per_sm(reinterpret_cast<const void *>(kernel), Cfg::kThreads, Cfg::kSmemBytes, dev, bps);
     if (st != B3G_OK) return st;
     const uint64_t grid = grid_for(a.n_tiles, bps, info.sm_count);
-    kernel<<<static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tmap, a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(Cfg::kThreads), Cfg::kSmemBytes,
+                               stream, tmap, a);
     return e == cudaSuccess ? B3G_OK : cuda_fail(e, "leaf_tma_kernel launch");
 }
 
@@ -679,8 +687,7 @@ b3g_status launch_direct(const LeafArgs &a, cudaStream_t stream, int dev, const 
     b3g_status st = kernel_blocks_per_sm(reinterpret_cast<const void *>(kernel), C, 0, dev, bps);
     if (st != B3G_OK) return st;
     const uint64_t grid = grid_for(a.n_tiles, bps, info.sm_count);
-    kernel<<<static_cast<unsigned>(grid), C, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(C), 0, stream, a);
     return e == cudaSuccess ? B3G_OK : cuda_fail(e, "leaf_direct_kernel launch");
 }
 
@@ -699,7 +706,7 @@ const char *kernel_config() {
     std::call_once(once, [] {
         std::snprintf(buf, sizeof buf,
                       "leaf_tma_kernel<%d,%d,%d> unroll=%d min_blocks=%d g_form=%d top_batch=%d pair_noinline=%d "
-                      "rot_fma=0x%x",
+                      "rot_fma=0x%x pdl=1",
                       1 << kDefaultLeavesLog2, Tuning<(1 << kDefaultLeavesLog2)>::S,
                       Tuning<(1 << kDefaultLeavesLog2)>::LOAD, kCopyLoopUnroll, B3G_MIN_BLOCKS, B3G_G_FORM,
                       B3G_TOP_BATCH, B3G_PAIR_NOINLINE, static_cast<unsigned>(B3G_ROT_FMA));

@@ -23,6 +23,10 @@ constexpr int kReduceMaxThreads = 512;
 
 __global__ void __launch_bounds__(kReduceMaxThreads) reduce_cvs_kernel(const ReduceArgs a) {
     __shared__ __align__(128) uint8_t node_mem[kReduceMaxThreads * 32];
+    // launched early behind the kernel that writes a.in: wait for its results, and let
+    // the next level's launch start early in turn
+    grid_dependency_wait();
+    launch_dependents();
     const uint32_t nodes = smem_u32(node_mem);
     uint32_t key[8];
 #pragma unroll
@@ -82,8 +86,10 @@ b3g_status launch_reduce(const ReduceArgs &a, cudaStream_t stream) {
     const uint64_t groups = (a.count + a.group - 1) / a.group;
     if (groups > 0x7fffffffull) return B3G_ERR_ARG;
     const int threads = a.group / 2 < 32 ? 32 : static_cast<int>(a.group / 2);
-    reduce_cvs_kernel<<<static_cast<unsigned>(groups), threads, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    // the launch overlaps the tail of the kernel ahead (the leaf kernel or the previous
+    // level), whose output it waits for
+    cudaError_t e = launch_pdl(reduce_cvs_kernel, dim3(static_cast<unsigned>(groups)),
+                               dim3(static_cast<unsigned>(threads)), 0, stream, a);
     return e == cudaSuccess ? B3G_OK : cuda_fail(e, "reduce_cvs_kernel launch");
 }
 
