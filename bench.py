@@ -115,18 +115,22 @@ class ClockSampler:
 
 
 def _traffic_per_launch(lib, nchunks):
-    """DRAM bytes of one leaf launch, scaled by chunks from the ncu capture recorded in
-    profiles/leaf_tma_kernel_traffic.json; None if that capture is of another kernel
-    configuration than the one built."""
+    """DRAM bytes and issued thread instructions of one leaf launch, scaled by chunks from
+    the ncu capture recorded in profiles/leaf_tma_kernel_traffic.json; None if that
+    capture is of another kernel configuration than the one built."""
     p = os.path.join(HERE, "profiles", "leaf_tma_kernel_traffic.json")
     if not os.path.exists(p):
-        return None, None
+        return None, None, None
     with open(p) as f:
         rec = json.load(f)
     if rec.get("kernel_config") != lib.blake3_kernel_config().decode():
-        return None, "capture is of another kernel configuration"
+        return None, "capture is of another kernel configuration", None
     per_chunk = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) / rec["chunks"]
-    return per_chunk * nchunks, f"ncu capture on {rec['workload']} scaled by chunks ({rec['chunks']} -> {nchunks})"
+    issued = None
+    if "warp_inst_executed" in rec:
+        issued = rec["warp_inst_executed"] * 32 / rec["chunks"] * nchunks
+    return (per_chunk * nchunks, f"ncu capture on {rec['workload']} scaled by chunks ({rec['chunks']} -> {nchunks})",
+            issued)
 
 
 def _max_over_ranks(x: float, world: int, device) -> float:
@@ -162,6 +166,41 @@ def _oracle_sample(host_bytes: torch.Tensor, key: bytes, target_s: float):
         if dt >= target_s or n >= host_bytes.numel():
             return n, dt
         n = min(host_bytes.numel(), n * max(2, int(target_s / max(dt, 1e-3) * 0.9)))
+
+
+def _oracle_threaded(host_bytes: torch.Tensor, key: bytes, threads: int):
+    """All host cores through the unchanged oracle functions: the largest power-of-two
+    prefix of whole chunks is split into equal aligned subtrees, hashed by parallel
+    threads (the ctypes calls release the GIL), and folded pairwise on one thread with
+    ROOT on the top parent.  Checked against the plain oracle on a small prefix first."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+
+    def digest(data, t):
+        chunks = data.numel() // 1024
+        per = chunks // t
+        with ThreadPoolExecutor(t) as ex:
+            cvs = list(ex.map(lambda i: oracle.subtree_cv(data[i * per * 1024:(i + 1) * per * 1024], key, i * per),
+                              range(t)))
+        while len(cvs) > 1:
+            cvs = [oracle.parent_cv(key, cvs[2 * j], cvs[2 * j + 1], len(cvs) == 2) for j in range(len(cvs) // 2)]
+        return cvs[0]
+
+    chunks = host_bytes.numel() // 1024
+    if chunks < 2 * threads:
+        return None
+    p2 = 1 << (chunks.bit_length() - 1)
+    t = 1 << (threads.bit_length() - 1)
+    check = host_bytes[:min(p2, 1 << 14) * 1024]
+    if digest(check, t) != oracle.keyed_hash(check, key):
+        raise RuntimeError("threaded oracle fold differs from the oracle")
+    data = host_bytes[:p2 * 1024]
+    t0 = time.perf_counter()
+    digest(data, t)
+    dt = time.perf_counter() - t0
+    return {"value": p2 * 1024 / dt / 1e9, "unit": "GB/s", "cores": t, "kind": "oracle, one thread per aligned subtree",
+            "sample": f"first {p2 * 1024} bytes of the workload as one input: {t} subtrees of {p2 // t} chunks "
+                      f"hashed in parallel by the unchanged oracle, folded on one thread ({dt:.1f} s)"}
 
 
 def run_reference(args):
@@ -274,6 +313,10 @@ def run_ours(args):
         torch.distributed.barrier()
     total_ms = starts[0].elapsed_time(end)
     leaf_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
+    step_ms = [starts[i].elapsed_time(starts[i + 1] if i + 1 < args.steps else end) for i in range(args.steps)]
+    timing = {"step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
+              "leaf_ms_median": statistics.median(leaf_ms),
+              "reduction_and_gaps_ms_median": statistics.median(s - l for s, l in zip(step_ms, leaf_ms))}
     total_ms = _max_over_ranks(total_ms, world, "cuda")
     ms_per_step = total_ms / args.steps
     value = _job_gbs(n, args.steps, total_ms, world)
@@ -304,9 +347,13 @@ def run_ours(args):
         "roofline_gbs": min(float(peaks.get("hbm_gbs", 6800.0)), int_peak / (ops / n) / 1e9),
     }
     roofline["frac_of_min_roofline"] = (n / leaf_s / 1e9) / roofline["roofline_gbs"]
-    traffic, traffic_src = _traffic_per_launch(lib, nchunks)
+    traffic, traffic_src, issued = _traffic_per_launch(lib, nchunks)
     roofline["traffic"] = traffic
     roofline["traffic_source"] = traffic_src
+    if issued is not None:
+        # the same peak against the instructions the kernel actually issues (ncu inst_executed)
+        roofline["issued"] = {"instructions_per_byte": issued / n, "achieved": issued / leaf_s / 1e9,
+                              "frac": issued / leaf_s / int_peak, "unit": "G instructions/s"}
     roofline["algorithmic_bytes"] = n
     roofline["kernel_config"] = lib.blake3_kernel_config().decode()
 
@@ -324,6 +371,9 @@ def run_ours(args):
         cpu = {"value": sample / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"first {sample} bytes of the workload hashed as one input by the single-threaded "
                          f"C oracle ({dt:.1f} s)"}
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        if cores > 1:
+            cpu["all_cores"] = _oracle_threaded(host, key, cores)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -332,7 +382,7 @@ def run_ours(args):
         "config": {"workload": f"{w.name} keyed BLAKE3, {w.kind} bytes seed {w.data_seed}, key seed {w.key_seed}",
                    "bytes": n, "chunks": nchunks, "leaves_per_cta": 1 << leaves_log2, "cta_roots": tiles,
                    "l2": f"input {n / 1e9:.2f} GB > 126 MB L2; no flush needed", "parallelism": f"replicas{world}"},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "timing": timing, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches * args.steps, "clocks": clocks,
         "digest": digest_api.hex(),
     }

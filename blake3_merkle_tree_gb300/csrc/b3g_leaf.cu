@@ -119,13 +119,18 @@ struct TmaCfg {
     static constexpr uint32_t kTopBatch = (CHUNK_CVS || C != 128) ? 0 : B3G_TOP_BATCH;
     static constexpr uint32_t kTopABytes = kTopBatch * 32 * 32;
     static constexpr uint32_t kTopBBytes = kTopBatch * 16 * 32;
-    // layout: [align 1024][rings][2 node buffers][scratch 1][scratch 2][top A][top B][barriers]
+    // The scratch buffers (a tile's own levels) and top B (the batched levels) are
+    // never in use at the same time: the reducer warp runs one or the other, so the
+    // scratch lives inside top B when it fits.
+    static constexpr bool kScratchInTopB = kTopBatch > 0 && kTopBBytes >= kScratch1Bytes + kScratch2Bytes;
+    // layout: [align 1024][rings][2 node buffers][top A][top B][scratch 1][scratch 2][barriers]
     static constexpr uint32_t kOffNodes = kConsumerWarps * kRingBytes;
-    static constexpr uint32_t kOffScratch1 = kOffNodes + 2 * kNodeBytes;
-    static constexpr uint32_t kOffScratch2 = kOffScratch1 + kScratch1Bytes;
-    static constexpr uint32_t kOffTopA = kOffScratch2 + kScratch2Bytes;
+    static constexpr uint32_t kOffTopA = kOffNodes + 2 * kNodeBytes;
     static constexpr uint32_t kOffTopB = kOffTopA + kTopABytes;
-    static constexpr uint32_t kOffBars = kOffTopB + kTopBBytes;
+    static constexpr uint32_t kOffScratch1 = kScratchInTopB ? kOffTopB : kOffTopB + kTopBBytes;
+    static constexpr uint32_t kOffScratch2 = kOffScratch1 + kScratch1Bytes;
+    static constexpr uint32_t kOffBars =
+        kScratchInTopB ? kOffTopB + kTopBBytes : kOffScratch2 + kScratch2Bytes;
     static constexpr uint32_t kNumBars = kConsumerWarps * S + 4;
     static constexpr size_t kSmemBytes = 1024 + size_t(kOffBars) + 8 * kNumBars;
     static_assert(S >= 2 && S <= kLoadsPerChunk, "stage count");
