@@ -62,10 +62,14 @@ def _load():
         lib.oracle_chunk_cvs.argtypes = [c_u8p, u64, u64, c_u8p, c_u8p]
         lib.oracle_blake2s_256.argtypes = [c_u8p, ctypes.c_size_t, c_u8p]
         lib.oracle_keyed_hash_xof.argtypes = [c_u8p, u64, c_u8p, c_u8p, u64]
+        lib.oracle_hash.argtypes = [c_u8p, u64, c_u8p]
+        lib.oracle_hash_recursive.argtypes = [c_u8p, u64, c_u8p]
+        lib.oracle_hash_xof.argtypes = [c_u8p, u64, c_u8p, u64]
         for name in ("oracle_iv", "oracle_msg_permutation", "oracle_flags", "oracle_compress",
                      "oracle_chunk_cv", "oracle_parent_cv", "oracle_keyed_hash",
                      "oracle_keyed_hash_recursive", "oracle_subtree_cv", "oracle_chunk_cvs",
-                     "oracle_blake2s_256", "oracle_keyed_hash_xof"):
+                     "oracle_blake2s_256", "oracle_keyed_hash_xof", "oracle_hash", "oracle_hash_recursive",
+                     "oracle_hash_xof"):
             getattr(lib, name).restype = None
         _lib = lib
         return lib
@@ -180,6 +184,34 @@ def keyed_hash_xof(data, key, out_len: int) -> bytes:
     p, n, keep = _buf(data)
     out = ctypes.create_string_buffer(max(1, out_len))
     _load().oracle_keyed_hash_xof(p, n, _key(key), out, out_len)
+    del keep
+    return out.raw[:out_len]
+
+
+def hash(data) -> bytes:  # noqa: A001 - the mode's name
+    """The 32-byte digest in the default (unkeyed) mode: the IV is the initial CV and no
+    compression carries KEYED_HASH (stack-merge tree)."""
+    p, n, keep = _buf(data)
+    out = ctypes.create_string_buffer(32)
+    _load().oracle_hash(p, n, out)
+    del keep
+    return out.raw
+
+
+def hash_recursive(data) -> bytes:
+    """The default-mode digest, recursive tree form."""
+    p, n, keep = _buf(data)
+    out = ctypes.create_string_buffer(32)
+    _load().oracle_hash_recursive(p, n, out)
+    del keep
+    return out.raw
+
+
+def hash_xof(data, out_len: int) -> bytes:
+    """out_len bytes of default-mode extendable output."""
+    p, n, keep = _buf(data)
+    out = ctypes.create_string_buffer(max(1, out_len))
+    _load().oracle_hash_xof(p, n, out, out_len)
     del keep
     return out.raw[:out_len]
 

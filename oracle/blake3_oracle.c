@@ -51,6 +51,8 @@
  *     message permutation, the flag bit values, the placement of counter / block
  *     length / flags in the state and the number of rounds (7) are taken from the
  *     specification as written and are checked only for internal consistency.
+ *     The default (unkeyed) mode shares all of that; what it adds, the IV as the
+ *     initial CV, is pinned with the IV; its flag word (no mode bit) is unpinned.
  *
  * Plain C11, scalar, no SIMD, no threads.
  */
@@ -169,7 +171,7 @@ static void compress_words(const uint32_t cv[8], const uint32_t block[16], uint6
 /* Leaf: the CV of one chunk (page section "BLAKE3", "压缩函数").                    */
 /* ------------------------------------------------------------------------------ */
 
-static void chunk_cv_words(const uint32_t key[8], const uint8_t *chunk, size_t chunk_len,
+static void chunk_cv_words(const uint32_t key[8], uint32_t mode, const uint8_t *chunk, size_t chunk_len,
                            uint64_t counter, int is_root, uint32_t out_cv[8]) {
     /* number of blocks: ceil(len/64), and one empty block for an empty chunk */
     size_t nblocks = chunk_len == 0 ? 1 : (chunk_len + BLOCK_LEN - 1) / BLOCK_LEN;
@@ -184,7 +186,7 @@ static void chunk_cv_words(const uint32_t key[8], const uint8_t *chunk, size_t c
         memset(padded, 0, sizeof padded);
         if (take) memcpy(padded, chunk + start, take);
         words_from_bytes(padded, 16, m);
-        uint32_t flags = F_KEYED_HASH;
+        uint32_t flags = mode;
         if (b == 0) flags |= F_CHUNK_START;
         if (b + 1 == nblocks) {
             flags |= F_CHUNK_END;
@@ -201,13 +203,13 @@ static void chunk_cv_words(const uint32_t key[8], const uint8_t *chunk, size_t c
 /* KEYED_HASH|PARENT, key as the input CV, left CV || right CV as the message.      */
 /* ------------------------------------------------------------------------------ */
 
-static void parent_cv_words(const uint32_t key[8], const uint32_t left[8], const uint32_t right[8],
+static void parent_cv_words(const uint32_t key[8], uint32_t mode, const uint32_t left[8], const uint32_t right[8],
                             int is_root, uint32_t out_cv[8]) {
     uint32_t m[16];
     uint32_t out[16];
     memcpy(m, left, 8 * sizeof(uint32_t));
     memcpy(m + 8, right, 8 * sizeof(uint32_t));
-    uint32_t flags = F_KEYED_HASH | F_PARENT | (is_root ? F_ROOT : 0u);
+    uint32_t flags = mode | F_PARENT | (is_root ? F_ROOT : 0u);
     compress_words(key, m, 0, BLOCK_LEN, flags, out);
     memcpy(out_cv, out, 8 * sizeof(uint32_t));
 }
@@ -233,19 +235,19 @@ static uint64_t largest_pow2_below(uint64_t n) { /* n >= 2 */
     return p;
 }
 
-static void subtree_words(const uint32_t key[8], const uint8_t *buf, uint64_t len,
+static void subtree_words(const uint32_t key[8], uint32_t mode, const uint8_t *buf, uint64_t len,
                           uint64_t first_chunk, uint64_t nchunks, uint64_t counter_base,
                           int is_root, uint32_t out_cv[8]) {
     if (nchunks == 1) {
-        chunk_cv_words(key, buf + first_chunk * CHUNK_LEN, chunk_bytes(len, first_chunk),
+        chunk_cv_words(key, mode, buf + first_chunk * CHUNK_LEN, chunk_bytes(len, first_chunk),
                        counter_base + first_chunk, is_root, out_cv);
         return;
     }
     uint64_t left_n = largest_pow2_below(nchunks);
     uint32_t l[8], r[8];
-    subtree_words(key, buf, len, first_chunk, left_n, counter_base, 0, l);
-    subtree_words(key, buf, len, first_chunk + left_n, nchunks - left_n, counter_base, 0, r);
-    parent_cv_words(key, l, r, is_root, out_cv);
+    subtree_words(key, mode, buf, len, first_chunk, left_n, counter_base, 0, l);
+    subtree_words(key, mode, buf, len, first_chunk + left_n, nchunks - left_n, counter_base, 0, r);
+    parent_cv_words(key, mode, l, r, is_root, out_cv);
 }
 
 /* ------------------------------------------------------------------------------ */
@@ -258,30 +260,30 @@ static void subtree_words(const uint32_t key[8], const uint8_t *buf, uint64_t le
 
 #define MAX_DEPTH 64
 
-static void stack_merge_words(const uint32_t key[8], const uint8_t *buf, uint64_t len,
+static void stack_merge_words(const uint32_t key[8], uint32_t mode, const uint8_t *buf, uint64_t len,
                               uint32_t out_cv[8]) {
     uint32_t stack[MAX_DEPTH + 1][8];
     int depth = 0;
     uint64_t n = num_chunks(len);
     if (n == 1) {
-        chunk_cv_words(key, buf, chunk_bytes(len, 0), 0, 1, out_cv);
+        chunk_cv_words(key, mode, buf, chunk_bytes(len, 0), 0, 1, out_cv);
         return;
     }
     for (uint64_t i = 0; i + 1 < n; i++) {
-        chunk_cv_words(key, buf + i * CHUNK_LEN, CHUNK_LEN, i, 0, stack[depth]);
+        chunk_cv_words(key, mode, buf + i * CHUNK_LEN, CHUNK_LEN, i, 0, stack[depth]);
         depth++;
         uint64_t c = i + 1;
         while ((c & 1) == 0) {
-            parent_cv_words(key, stack[depth - 2], stack[depth - 1], 0, stack[depth - 2]);
+            parent_cv_words(key, mode, stack[depth - 2], stack[depth - 1], 0, stack[depth - 2]);
             depth--;
             c >>= 1;
         }
     }
     /* the last chunk, then the right-to-left fold */
     uint32_t right[8];
-    chunk_cv_words(key, buf + (n - 1) * CHUNK_LEN, chunk_bytes(len, n - 1), n - 1, 0, right);
+    chunk_cv_words(key, mode, buf + (n - 1) * CHUNK_LEN, chunk_bytes(len, n - 1), n - 1, 0, right);
     while (depth > 0) {
-        parent_cv_words(key, stack[depth - 1], right, depth == 1, right);
+        parent_cv_words(key, mode, stack[depth - 1], right, depth == 1, right);
         depth--;
     }
     memcpy(out_cv, right, sizeof right);
@@ -301,7 +303,8 @@ typedef struct {
     uint32_t flags; /* without ROOT */
 } root_inputs;
 
-static void root_of_chunk(const uint32_t key[8], const uint8_t *chunk, size_t chunk_len, root_inputs *out) {
+static void root_of_chunk(const uint32_t key[8], uint32_t mode, const uint8_t *chunk, size_t chunk_len,
+                          root_inputs *out) {
     size_t nblocks = chunk_len == 0 ? 1 : (chunk_len + BLOCK_LEN - 1) / BLOCK_LEN;
     uint32_t cv[8];
     memcpy(cv, key, sizeof cv);
@@ -313,7 +316,7 @@ static void root_of_chunk(const uint32_t key[8], const uint8_t *chunk, size_t ch
         memset(padded, 0, sizeof padded);
         if (take) memcpy(padded, chunk + start, take);
         words_from_bytes(padded, 16, m);
-        uint32_t flags = F_KEYED_HASH | (b == 0 ? F_CHUNK_START : 0u);
+        uint32_t flags = mode | (b == 0 ? F_CHUNK_START : 0u);
         if (b + 1 == nblocks) {
             memcpy(out->cv, cv, sizeof cv);
             memcpy(out->block, m, sizeof m);
@@ -329,30 +332,28 @@ static void root_of_chunk(const uint32_t key[8], const uint8_t *chunk, size_t ch
 
 /* Root inputs of the whole input: the single chunk's last block, or the top
  * parent whose children are the largest power-of-two left subtree and the rest. */
-static void root_inputs_of(const uint32_t key[8], const uint8_t *buf, uint64_t len, root_inputs *out) {
+static void root_inputs_of(const uint32_t key[8], uint32_t mode, const uint8_t *buf, uint64_t len,
+                           root_inputs *out) {
     uint64_t n = num_chunks(len);
     if (n == 1) {
-        root_of_chunk(key, buf, chunk_bytes(len, 0), out);
+        root_of_chunk(key, mode, buf, chunk_bytes(len, 0), out);
         return;
     }
     uint64_t left_n = largest_pow2_below(n);
     uint32_t l[8], r[8];
-    subtree_words(key, buf, len, 0, left_n, 0, 0, l);
-    subtree_words(key, buf, len, left_n, n - left_n, 0, 0, r);
+    subtree_words(key, mode, buf, len, 0, left_n, 0, 0, l);
+    subtree_words(key, mode, buf, len, left_n, n - left_n, 0, 0, r);
     memcpy(out->cv, key, 8 * sizeof(uint32_t));
     memcpy(out->block, l, 8 * sizeof(uint32_t));
     memcpy(out->block + 8, r, 8 * sizeof(uint32_t));
     out->block_len = BLOCK_LEN;
-    out->flags = F_KEYED_HASH | F_PARENT;
+    out->flags = mode | F_PARENT;
 }
 
-/* out_len bytes of extendable output; the first 32 equal oracle_keyed_hash. */
-void oracle_keyed_hash_xof(const uint8_t *buf, uint64_t len, const uint8_t key[32], uint8_t *out,
-                           uint64_t out_len) {
-    uint32_t k[8];
-    words_from_bytes(key, 8, k);
+static void xof_words(const uint32_t key[8], uint32_t mode, const uint8_t *buf, uint64_t len, uint8_t *out,
+                      uint64_t out_len) {
     root_inputs ri;
-    root_inputs_of(k, buf, len, &ri);
+    root_inputs_of(key, mode, buf, len, &ri);
     for (uint64_t i = 0; i * 64 < out_len; i++) {
         uint32_t o[16];
         uint8_t blk[64];
@@ -361,6 +362,38 @@ void oracle_keyed_hash_xof(const uint8_t *buf, uint64_t len, const uint8_t key[3
         uint64_t take = out_len - i * 64 < 64 ? out_len - i * 64 : 64;
         memcpy(out + i * 64, blk, (size_t)take);
     }
+}
+
+/* out_len bytes of extendable output; the first 32 equal oracle_keyed_hash. */
+void oracle_keyed_hash_xof(const uint8_t *buf, uint64_t len, const uint8_t key[32], uint8_t *out,
+                           uint64_t out_len) {
+    uint32_t k[8];
+    words_from_bytes(key, 8, k);
+    xof_words(k, F_KEYED_HASH, buf, len, out, out_len);
+}
+
+/* ------------------------------------------------------------------------------ */
+/* The default (unkeyed) mode.  Page section "BLAKE3": the first block of a chunk   */
+/* starts from an IV by default, from the user's key in keyed mode.  Following the */
+/* specification's hash mode, the default mode starts every chunk and every parent */
+/* from the IV and sets no mode flag (keyed mode adds KEYED_HASH to every          */
+/* compression); the tree and everything else are the same.                       */
+/* ------------------------------------------------------------------------------ */
+
+void oracle_hash(const uint8_t *buf, uint64_t len, uint8_t out[32]) {
+    uint32_t cv[8];
+    stack_merge_words(ORACLE_IV, 0u, buf, len, cv);
+    bytes_from_words(cv, 8, out);
+}
+
+void oracle_hash_recursive(const uint8_t *buf, uint64_t len, uint8_t out[32]) {
+    uint32_t cv[8];
+    subtree_words(ORACLE_IV, 0u, buf, len, 0, num_chunks(len), 0, 1, cv);
+    bytes_from_words(cv, 8, out);
+}
+
+void oracle_hash_xof(const uint8_t *buf, uint64_t len, uint8_t *out, uint64_t out_len) {
+    xof_words(ORACLE_IV, 0u, buf, len, out, out_len);
 }
 
 /* ------------------------------------------------------------------------------ */
@@ -428,7 +461,7 @@ void oracle_chunk_cv(const uint8_t key[32], const uint8_t *chunk, size_t chunk_l
                      uint64_t counter, int is_root, uint8_t out[32]) {
     uint32_t k[8], cv[8];
     words_from_bytes(key, 8, k);
-    chunk_cv_words(k, chunk, chunk_len, counter, is_root, cv);
+    chunk_cv_words(k, F_KEYED_HASH, chunk, chunk_len, counter, is_root, cv);
     bytes_from_words(cv, 8, out);
 }
 
@@ -438,7 +471,7 @@ void oracle_parent_cv(const uint8_t key[32], const uint8_t left[32], const uint8
     words_from_bytes(key, 8, k);
     words_from_bytes(left, 8, l);
     words_from_bytes(right, 8, r);
-    parent_cv_words(k, l, r, is_root, o);
+    parent_cv_words(k, F_KEYED_HASH, l, r, is_root, o);
     bytes_from_words(o, 8, out);
 }
 
@@ -446,7 +479,7 @@ void oracle_parent_cv(const uint8_t key[32], const uint8_t left[32], const uint8
 void oracle_keyed_hash(const uint8_t *buf, uint64_t len, const uint8_t key[32], uint8_t out[32]) {
     uint32_t k[8], cv[8];
     words_from_bytes(key, 8, k);
-    stack_merge_words(k, buf, len, cv);
+    stack_merge_words(k, F_KEYED_HASH, buf, len, cv);
     bytes_from_words(cv, 8, out);
 }
 
@@ -455,7 +488,7 @@ void oracle_keyed_hash_recursive(const uint8_t *buf, uint64_t len, const uint8_t
                                  uint8_t out[32]) {
     uint32_t k[8], cv[8];
     words_from_bytes(key, 8, k);
-    subtree_words(k, buf, len, 0, num_chunks(len), 0, 1, cv);
+    subtree_words(k, F_KEYED_HASH, buf, len, 0, num_chunks(len), 0, 1, cv);
     bytes_from_words(cv, 8, out);
 }
 
@@ -465,7 +498,7 @@ void oracle_subtree_cv(const uint8_t *buf, uint64_t len, uint64_t chunk_offset,
                        const uint8_t key[32], int is_root, uint8_t out[32]) {
     uint32_t k[8], cv[8];
     words_from_bytes(key, 8, k);
-    subtree_words(k, buf, len, 0, num_chunks(len), chunk_offset, is_root, cv);
+    subtree_words(k, F_KEYED_HASH, buf, len, 0, num_chunks(len), chunk_offset, is_root, cv);
     bytes_from_words(cv, 8, out);
 }
 
@@ -477,7 +510,7 @@ void oracle_chunk_cvs(const uint8_t *buf, uint64_t len, uint64_t chunk_offset,
     words_from_bytes(key, 8, k);
     uint64_t n = num_chunks(len);
     for (uint64_t i = 0; i < n; i++) {
-        chunk_cv_words(k, buf + i * CHUNK_LEN, chunk_bytes(len, i), chunk_offset + i, 0, cv);
+        chunk_cv_words(k, F_KEYED_HASH, buf + i * CHUNK_LEN, chunk_bytes(len, i), chunk_offset + i, 0, cv);
         bytes_from_words(cv, 8, out + 32 * i);
     }
 }

@@ -229,3 +229,60 @@ def test_xof_block_is_the_root_compression_with_counter():
     for i in range(5):
         blk = oracle.compress(KEY, left + right, i, 64, f["KEYED_HASH"] | f["PARENT"] | f["ROOT"])
         assert out[64 * i:64 * (i + 1)] == blk
+
+
+# ---------------------------------------------------------------------------------
+# The default (unkeyed) mode (page section "BLAKE3": the initial chaining value is an
+# IV by default, the user's key in keyed mode).  Its IV is pinned by the closed form
+# above; its flag word (no mode bit) is unpinned like the other flag values.
+# ---------------------------------------------------------------------------------
+
+def _iv_bytes():
+    return b"".join(w.to_bytes(4, "little") for w in oracle.iv())
+
+
+@pytest.mark.parametrize("n", [0, 1, 64, 65, 1023, 1024])
+def test_default_mode_one_chunk_identity(n):
+    """len <= 1024: the IV-started block chain of the single chunk, no mode bit, ROOT last."""
+    f = oracle.flags()
+    data = _data(n, seed=700 + n).tobytes()
+    cv = _iv_bytes()
+    nblocks = max(1, -(-n // 64))
+    for b in range(nblocks):
+        part = data[64 * b:64 * (b + 1)]
+        flags = (f["CHUNK_START"] if b == 0 else 0) | (f["CHUNK_END"] | f["ROOT"] if b == nblocks - 1 else 0)
+        cv = oracle.compress(cv, part.ljust(64, b"\0"), 0, len(part), flags)[:32]
+    assert cv == oracle.hash(data)
+
+
+def test_default_mode_tree_forms_agree():
+    """Recursive split == stack merge in the default mode on every length class."""
+    for n in [0, 1, 1024, 1025, 2048, 3 * 1024 + 1, 8 * 1024, 13 * 1024 + 7, 64 * 1024 - 1, 100 * 1024 + 3]:
+        data = _data(n, seed=800 + n).tobytes()
+        assert oracle.hash(data) == oracle.hash_recursive(data), n
+
+
+def test_default_mode_parent_uses_iv_and_no_mode_bit():
+    """Two chunks: the root is the parent of the two chunk CVs, started from the IV."""
+    f = oracle.flags()
+    data = _data(2048, seed=901).tobytes()
+    iv = _iv_bytes()
+
+    def chunk(c, ctr):
+        cv = iv
+        for b in range(16):
+            flags = (f["CHUNK_START"] if b == 0 else 0) | (f["CHUNK_END"] if b == 15 else 0)
+            cv = oracle.compress(cv, c[64 * b:64 * b + 64], ctr, 64, flags)[:32]
+        return cv
+
+    left, right = chunk(data[:1024], 0), chunk(data[1024:], 1)
+    root = oracle.compress(iv, left + right, 0, 64, f["PARENT"] | f["ROOT"])[:32]
+    assert root == oracle.hash(data)
+
+
+@pytest.mark.parametrize("n", [0, 5, 1024, 4097])
+def test_default_mode_differs_from_keyed_with_iv_key_and_has_xof_prefix(n):
+    data = _data(n, seed=950 + n).tobytes()
+    assert oracle.hash(data) != oracle.keyed_hash(data, _iv_bytes())  # the mode bit is in every compression
+    assert oracle.hash_xof(data, 32) == oracle.hash(data)
+    assert oracle.hash_xof(data, 200)[:100] == oracle.hash_xof(data, 100)
