@@ -482,6 +482,19 @@ def run_mode(args):
                 "value": d.numel() / ms / 1e6, "unit": "GB/s", "ms_per_digest": ms,
                 "one_shot_GBps": d.numel() / ms_one / 1e6,
                 "config": {"workload": w.name, "segment_bytes": seg, "segments": -(-d.numel() // seg)}}
+    elif args.mode == "default":
+        # the default (unkeyed) mode on the same workload, through the public one-shot
+        # call, beside the keyed call
+        w = workloads.WORKLOADS[args.workload]
+        d = w.data(device="cuda")
+        out32 = torch.empty(32, dtype=torch.uint8, device="cuda")
+        ws = torch.empty(max(16, binding.blake3_workspace_size(d.numel())), dtype=torch.uint8, device="cuda")
+        ms = _timed(lambda: binding.blake3_hash_ws(d, ws, out=out32), args.steps, args.warmup)
+        ms_keyed = _timed(lambda: binding.blake3_keyed_hash_ws(d, w.key(), ws, out=out32), args.steps, args.warmup)
+        line = {"mode": "default", "metric": "GB/s hashed in the default (unkeyed) mode (BLAKE3, 1 GB300)",
+                "value": d.numel() / ms / 1e6, "unit": "GB/s", "ms_per_digest": ms,
+                "keyed_GBps": d.numel() / ms_keyed / 1e6,
+                "config": {"workload": w.name, "call": "blake3_hash_ws / blake3_keyed_hash_ws"}}
     else:  # small: the 1 MiB digest, per call and replayed from a CUDA graph
         w = workloads.WORKLOADS["1MiB"]
         d = w.data(device="cuda")
@@ -538,7 +551,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--mode", choices=["headline", "xof", "stream", "small"], default="headline")
+    ap.add_argument("--mode", choices=["headline", "xof", "stream", "small", "default"], default="headline")
     ap.add_argument("--xof-bytes", type=int, default=1 << 32)
     ap.add_argument("--segment-bytes", type=int, default=(256 << 20) + 777)
     args = ap.parse_args()

@@ -1,4 +1,5 @@
-"""GB300-native keyed BLAKE3 digest of one buffer resident in device memory.
+"""GB300-native BLAKE3 digest (keyed, or the default unkeyed mode) of one buffer resident in
+device memory.
 
 The work runs in hand-written sm_103a CUDA kernels behind the C ABI declared in
 ``include/blake3_gb300.h`` (``libb3g.so``).  ``binding`` is a thin ctypes layer
@@ -18,6 +19,10 @@ _BINDING_NAMES = (
     "blake3_keyed_hash_noalloc",
     "blake3_keyed_hash_xof",
     "blake3_keyed_hash_host",
+    "blake3_hash",
+    "blake3_hash_ws",
+    "blake3_hash_xof",
+    "blake3_hash_host",
     "Hasher",
     "blake3_workspace_size",
     "blake3_keyed_chunk_cvs",

@@ -71,6 +71,11 @@ def library() -> ctypes.CDLL:
             "blake3_hasher_update": (i32, [vp, vp, u64, vp]),
             "blake3_hasher_finalize": (i32, [vp, vp, u64, vp]),
             "blake3_keyed_hash_host": (i32, [vp, u64, vp, vp, vp, sz, vp]),
+            "blake3_hash": (i32, [vp, u64, vp, vp]),
+            "blake3_hash_ws": (i32, [vp, u64, vp, vp, sz, vp]),
+            "blake3_hash_xof": (i32, [vp, u64, vp, u64, vp]),
+            "blake3_hasher_new_default": (i32, [ctypes.POINTER(vp)]),
+            "blake3_hash_host": (i32, [vp, u64, vp, vp, sz, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -153,6 +158,25 @@ def blake3_keyed_hash_ws(data: torch.Tensor, key, workspace: torch.Tensor | None
     st = library().blake3_keyed_hash_ws(_dev_ptr(data, "data"), _nbytes(data), _key(key), _dev_ptr(out, "out"),
                                         ws_ptr, ws_bytes, _stream(stream))
     _check(st, "blake3_keyed_hash_ws")
+    return out
+
+
+def blake3_hash(data: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Default-mode (unkeyed) digest of the contiguous CUDA tensor `data`."""
+    out = _out32(out, data)
+    st = library().blake3_hash(_dev_ptr(data, "data"), _nbytes(data), _dev_ptr(out, "out"), _stream(stream))
+    _check(st, "blake3_hash")
+    return out
+
+
+def blake3_hash_ws(data: torch.Tensor, workspace: torch.Tensor | None, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    out = _out32(out, data)
+    ws_ptr = _dev_ptr(workspace, "workspace") if workspace is not None else None
+    ws_bytes = _nbytes(workspace) if workspace is not None else 0
+    st = library().blake3_hash_ws(_dev_ptr(data, "data"), _nbytes(data), _dev_ptr(out, "out"), ws_ptr, ws_bytes,
+                                  _stream(stream))
+    _check(st, "blake3_hash_ws")
     return out
 
 
@@ -251,12 +275,29 @@ def blake3_keyed_hash_xof(data: torch.Tensor, key, out_len: int, out: torch.Tens
     return out
 
 
-class Hasher:
-    """Streaming keyed hasher over device segments (blake3_hasher_* of the C ABI)."""
+def blake3_hash_xof(data: torch.Tensor, out_len: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out_len bytes of default-mode (unkeyed) extendable output."""
+    if out is None:
+        dev = data.device if data.is_cuda else torch.device("cuda")
+        out = torch.empty(out_len, dtype=torch.uint8, device=dev)
+    if _nbytes(out) < out_len:
+        raise ValueError("output too small")
+    st = library().blake3_hash_xof(_dev_ptr(data, "data"), _nbytes(data), _dev_ptr(out, "out") if out_len else None,
+                                   out_len, _stream(stream))
+    _check(st, "blake3_hash_xof")
+    return out
 
-    def __init__(self, key):
+
+class Hasher:
+    """Streaming hasher over device segments (blake3_hasher_* of the C ABI): keyed with
+    `key`, or in the default (unkeyed) mode when `key` is None."""
+
+    def __init__(self, key=None):
         self._h = ctypes.c_void_p()
-        _check(library().blake3_hasher_new(_key(key), ctypes.byref(self._h)), "blake3_hasher_new")
+        if key is None:
+            _check(library().blake3_hasher_new_default(ctypes.byref(self._h)), "blake3_hasher_new_default")
+        else:
+            _check(library().blake3_hasher_new(_key(key), ctypes.byref(self._h)), "blake3_hasher_new")
 
     def update(self, data: torch.Tensor, stream=None) -> "Hasher":
         _check(library().blake3_hasher_update(self._h, _dev_ptr(data, "data"), _nbytes(data), _stream(stream)),
@@ -302,6 +343,20 @@ def blake3_keyed_hash_host(data: torch.Tensor, key, staging: torch.Tensor | None
     st = library().blake3_keyed_hash_host(t.data_ptr() if t.numel() else None, _nbytes(t), _key(key), out,
                                           st_ptr, st_bytes, _stream(stream))
     _check(st, "blake3_keyed_hash_host")
+    return out.raw
+
+
+def blake3_hash_host(data: torch.Tensor, staging: torch.Tensor | None = None, stream=None) -> bytes:
+    """Default-mode (unkeyed) digest of a contiguous HOST tensor; see blake3_keyed_hash_host."""
+    if data.is_cuda:
+        raise ValueError("data must be a host tensor")
+    t = data.contiguous()
+    out = ctypes.create_string_buffer(32)
+    st_ptr = _dev_ptr(staging, "staging") if staging is not None else None
+    st_bytes = _nbytes(staging) if staging is not None else 0
+    st = library().blake3_hash_host(t.data_ptr() if t.numel() else None, _nbytes(t), out, st_ptr, st_bytes,
+                                    _stream(stream))
+    _check(st, "blake3_hash_host")
     return out.raw
 
 

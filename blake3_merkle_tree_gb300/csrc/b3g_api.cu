@@ -80,8 +80,8 @@ size_t reduce_ws(uint64_t count, int g) {
 }
 
 // Reduce `count` CVs at d_cvs into d_out32 (see blake3_keyed_reduce_cvs).
-b3g_status reduce_levels(const uint8_t *d_cvs, uint64_t count, const uint32_t key[8], bool is_root, int g,
-                         uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
+b3g_status reduce_levels(const uint8_t *d_cvs, uint64_t count, const uint32_t key[8], uint32_t mode_flags,
+                         bool is_root, int g, uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
     if (count == 1) {
         cudaError_t e = cudaMemcpyAsync(d_out32, d_cvs, 32, cudaMemcpyDeviceToDevice, stream);
         return e == cudaSuccess ? B3G_OK : cuda_fail(e, "cudaMemcpyAsync");
@@ -97,6 +97,7 @@ b3g_status reduce_levels(const uint8_t *d_cvs, uint64_t count, const uint32_t ke
         const uint64_t groups = ceil_div(c, group);
         ra.out = groups == 1 ? d_out32 : next_buf;
         std::memcpy(ra.key, key, sizeof ra.key);
+        ra.mode_flags = mode_flags;
         ra.root = is_root ? 1u : 0u;
         ra.group = static_cast<uint32_t>(group);
         b3g_status st = launch_reduce(ra, stream);
@@ -108,8 +109,8 @@ b3g_status reduce_levels(const uint8_t *d_cvs, uint64_t count, const uint32_t ke
     }
 }
 
-LeafArgs leaf_args(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32], int t,
-                   bool root, uint8_t *out, uint32_t *status) {
+LeafArgs leaf_args(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
+                   uint32_t mode_flags, int t, bool root, uint8_t *out, uint32_t *status) {
     LeafArgs a;
     a.in = static_cast<const uint8_t *>(d_in);
     a.len = len;
@@ -121,6 +122,7 @@ LeafArgs leaf_args(const void *d_in, uint64_t len, uint64_t chunk_offset, const 
     a.status = status;
     a.wait_limit_ns = kWaitLimitNs;
     key_words(key, a.key);
+    a.mode_flags = mode_flags;
     a.root = root ? 1u : 0u;
     a.tail_bytes = static_cast<uint32_t>(len % kChunkBytes);
     a.ticket = nullptr;
@@ -154,13 +156,13 @@ bool fused_path(const void *d_in, uint64_t n_full) {
 
 // The whole path: leaf kernel, then the reduction levels.  `ws` must hold
 // blake3_workspace_size(len) bytes when more than one tile exists.
-b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32], bool root,
-                      uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
+b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
+                      uint32_t mode_flags, bool root, uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
     uint32_t *status = nullptr;
     b3g_status st = status_word(&status);
     if (st != B3G_OK) return st;
     const int t = choose_leaves_log2(n_chunks_of(len));
-    LeafArgs a = leaf_args(d_in, len, chunk_offset, key, t, root, nullptr, status);
+    LeafArgs a = leaf_args(d_in, len, chunk_offset, key, mode_flags, t, root, nullptr, status);
     if (a.n_tiles == 1) {
         a.out = d_out32;
         return launch_leaf(a, t, false, stream);
@@ -177,7 +179,7 @@ b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, con
     }
     st = launch_leaf(a, t, false, stream);
     if (st != B3G_OK) return st;
-    return reduce_levels(ws, a.n_tiles, a.key, root, kDefaultGroupLog2, d_out32,
+    return reduce_levels(ws, a.n_tiles, a.key, mode_flags, root, kDefaultGroupLog2, d_out32,
                          ws + round16(a.n_tiles * 32), stream);
 }
 
@@ -192,14 +194,15 @@ size_t hash_workspace(uint64_t len) {
 
 // Runs hash_range with a stream-ordered temporary workspace.
 b3g_status hash_range_alloc(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
-                            bool root, uint8_t *d_out32, cudaStream_t stream) {
+                            uint32_t mode_flags, bool root, uint8_t *d_out32, cudaStream_t stream) {
     const size_t need = hash_workspace(len);
     void *ws = nullptr;
     if (need) {
         cudaError_t e = cudaMallocAsync(&ws, need, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
     }
-    b3g_status st = hash_range(d_in, len, chunk_offset, key, root, d_out32, static_cast<uint8_t *>(ws), stream);
+    b3g_status st =
+        hash_range(d_in, len, chunk_offset, key, mode_flags, root, d_out32, static_cast<uint8_t *>(ws), stream);
     if (ws) {
         cudaError_t e = cudaFreeAsync(ws, stream);
         if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
@@ -211,9 +214,16 @@ b3g_status hash_range_alloc(const void *d_in, uint64_t len, uint64_t chunk_offse
 
 b3g_status device_status_word(uint32_t **out) { return status_word(out); }
 
-b3g_status hash_range_ws(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32], bool root,
-                         uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
-    return hash_range(d_in, len, chunk_offset, key, root, d_out32, ws, stream);
+b3g_status hash_range_ws(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
+                         uint32_t mode_flags, bool root, uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
+    return hash_range(d_in, len, chunk_offset, key, mode_flags, root, d_out32, ws, stream);
+}
+
+b3g_status reduce_cvs_ws(const uint8_t *d_cvs, uint64_t count, const uint32_t key[8], uint32_t mode_flags,
+                         bool root, uint8_t *d_out32, uint8_t *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (count == 0 || (count == 1 && root)) return B3G_ERR_ARG;
+    if (ws_bytes < reduce_ws(count, kDefaultGroupLog2)) return B3G_ERR_WORKSPACE;
+    return reduce_levels(d_cvs, count, key, mode_flags, root, kDefaultGroupLog2, d_out32, ws, stream);
 }
 
 b3g_status cuda_fail(cudaError_t err, const char *what) {
@@ -262,7 +272,7 @@ b3g_status blake3_keyed_hash(const void *d_in, uint64_t len, const uint8_t key[3
                              b3g_stream_t stream) {
     if (!key || !d_out32 || (!d_in && len > 0)) return B3G_ERR_NULL;
     if (misaligned16(d_out32)) return B3G_ERR_ALIGN;
-    return hash_range_alloc(d_in, len, 0, key, true, d_out32, reinterpret_cast<cudaStream_t>(stream));
+    return hash_range_alloc(d_in, len, 0, key, kModeKeyed, true, d_out32, reinterpret_cast<cudaStream_t>(stream));
 }
 
 b3g_status blake3_keyed_hash_ws(const void *d_in, uint64_t len, const uint8_t key[32], uint8_t *d_out32,
@@ -274,7 +284,30 @@ b3g_status blake3_keyed_hash_ws(const void *d_in, uint64_t len, const uint8_t ke
         if (!d_ws || ws_bytes < need) return B3G_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(d_ws) & 15u) return B3G_ERR_ALIGN;
     }
-    return hash_range(d_in, len, 0, key, true, d_out32, static_cast<uint8_t *>(d_ws),
+    return hash_range(d_in, len, 0, key, kModeKeyed, true, d_out32, static_cast<uint8_t *>(d_ws),
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+b3g_status blake3_hash(const void *d_in, uint64_t len, uint8_t *d_out32, b3g_stream_t stream) {
+    if (!d_out32 || (!d_in && len > 0)) return B3G_ERR_NULL;
+    if (misaligned16(d_out32)) return B3G_ERR_ALIGN;
+    uint8_t iv[32];
+    iv_key_bytes(iv);
+    return hash_range_alloc(d_in, len, 0, iv, kModeDefault, true, d_out32, reinterpret_cast<cudaStream_t>(stream));
+}
+
+b3g_status blake3_hash_ws(const void *d_in, uint64_t len, uint8_t *d_out32, void *d_ws, size_t ws_bytes,
+                          b3g_stream_t stream) {
+    if (!d_out32 || (!d_in && len > 0)) return B3G_ERR_NULL;
+    if (misaligned16(d_out32)) return B3G_ERR_ALIGN;
+    const size_t need = hash_workspace(len);
+    if (need) {
+        if (!d_ws || ws_bytes < need) return B3G_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(d_ws) & 15u) return B3G_ERR_ALIGN;
+    }
+    uint8_t iv[32];
+    iv_key_bytes(iv);
+    return hash_range(d_in, len, 0, iv, kModeDefault, true, d_out32, static_cast<uint8_t *>(d_ws),
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -285,7 +318,7 @@ b3g_status blake3_keyed_chunk_cvs(const void *d_in, uint64_t len, uint64_t chunk
     uint32_t *status = nullptr;
     b3g_status st = status_word(&status);
     if (st != B3G_OK) return st;
-    LeafArgs a = leaf_args(d_in, len, chunk_offset, key, kDefaultLeavesLog2, false, d_cvs, status);
+    LeafArgs a = leaf_args(d_in, len, chunk_offset, key, kModeKeyed, kDefaultLeavesLog2, false, d_cvs, status);
     return launch_leaf(a, kDefaultLeavesLog2, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -297,7 +330,7 @@ b3g_status blake3_keyed_subtree_root(const void *d_in, uint64_t len, uint64_t ch
     uint64_t p = 1;
     while (p < n) p <<= 1;
     if (chunk_offset % p != 0) return B3G_ERR_ALIGN;
-    return hash_range_alloc(d_in, len, chunk_offset, key, is_root != 0, d_out32,
+    return hash_range_alloc(d_in, len, chunk_offset, key, kModeKeyed, is_root != 0, d_out32,
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -316,7 +349,7 @@ b3g_status blake3_keyed_tile_roots(const void *d_in, uint64_t len, uint64_t chun
     uint32_t *status = nullptr;
     b3g_status st = status_word(&status);
     if (st != B3G_OK) return st;
-    LeafArgs a = leaf_args(d_in, len, chunk_offset, key, leaves_log2, is_root != 0, d_roots, status);
+    LeafArgs a = leaf_args(d_in, len, chunk_offset, key, kModeKeyed, leaves_log2, is_root != 0, d_roots, status);
     return launch_leaf(a, leaves_log2, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -341,8 +374,8 @@ b3g_status blake3_keyed_reduce_cvs(const uint8_t *d_cvs, uint64_t count, const u
     }
     uint32_t kw[8];
     key_words(key, kw);
-    return reduce_levels(d_cvs, count, kw, is_root != 0, group_log2, d_out32, static_cast<uint8_t *>(d_ws),
-                         reinterpret_cast<cudaStream_t>(stream));
+    return reduce_levels(d_cvs, count, kw, kModeKeyed, is_root != 0, group_log2, d_out32,
+                         static_cast<uint8_t *>(d_ws), reinterpret_cast<cudaStream_t>(stream));
 }
 
 b3g_status blake3_device_status(uint32_t *status_out) {

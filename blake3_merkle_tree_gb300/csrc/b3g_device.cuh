@@ -176,9 +176,11 @@ __device__ __forceinline__ void compress_full(const uint32_t cv[8], const uint32
     }
 }
 
-// Parent node: key as CV, left || right as the message.
-__device__ __forceinline__ void parent(const uint32_t key[8], const uint32_t l[8], const uint32_t r[8],
-                                       bool root, uint32_t out[8]) {
+// Parent node: key as CV, left || right as the message.  `mode_flags` is the flag bit
+// every compression of the hash mode carries: KEYED_HASH in keyed mode, none in the
+// default mode (whose `key` is the IV).
+__device__ __forceinline__ void parent(const uint32_t key[8], uint32_t mode_flags, const uint32_t l[8],
+                                       const uint32_t r[8], bool root, uint32_t out[8]) {
     uint32_t m[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -188,7 +190,7 @@ __device__ __forceinline__ void parent(const uint32_t key[8], const uint32_t l[8
     uint32_t cv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) cv[i] = key[i];
-    compress(cv, m, 0u, 0u, kBlockLen, kKeyedHash | kParent | (root ? kRoot : 0u));
+    compress(cv, m, 0u, 0u, kBlockLen, mode_flags | kParent | (root ? kRoot : 0u));
 #pragma unroll
     for (int i = 0; i < 8; ++i) out[i] = cv[i];
 }
@@ -393,7 +395,8 @@ __device__ __forceinline__ void load_node(uint32_t base, uint32_t j, uint32_t cv
 // ---------------------------------------------------------------------------------
 
 // Warp-level part: lane j holds node j (j < cnt); on return lane 0 holds the root.
-__device__ __forceinline__ void warp_tree(uint32_t x[8], uint32_t cnt, const uint32_t key[8], bool root) {
+__device__ __forceinline__ void warp_tree(uint32_t x[8], uint32_t cnt, const uint32_t key[8], uint32_t mode_flags,
+                                          bool root) {
     const uint32_t lane = threadIdx.x & 31u;
     while (cnt > 1) {
         const uint32_t half = cnt >> 1;
@@ -404,7 +407,7 @@ __device__ __forceinline__ void warp_tree(uint32_t x[8], uint32_t cnt, const uin
             r[w] = __shfl_sync(0xffffffffu, x[w], (2 * lane + 1) & 31u);
         }
         if (lane < half) {
-            parent(key, l, r, root && cnt == 2, x);
+            parent(key, mode_flags, l, r, root && cnt == 2, x);
         } else if (lane == half && (cnt & 1u)) {
 #pragma unroll
             for (int w = 0; w < 8; ++w) x[w] = l[w];  // node cnt-1 moves up
@@ -418,8 +421,8 @@ __device__ __forceinline__ void warp_tree(uint32_t x[8], uint32_t cnt, const uin
 // visible.  On return lane 0 of warp 0 (thread 0) holds the root in out[8]; the
 // node buffer may be reused after the call.
 __device__ __forceinline__ void block_tree(uint32_t nodes, uint32_t cnt, uint32_t tid, uint32_t nthreads,
-                                           uint32_t bar_id, const uint32_t key[8], bool root,
-                                           uint32_t out[8]) {
+                                           uint32_t bar_id, const uint32_t key[8], uint32_t mode_flags,
+                                           bool root, uint32_t out[8]) {
     while (cnt > 32) {
         const uint32_t half = cnt >> 1;
         uint32_t res[8];
@@ -428,7 +431,7 @@ __device__ __forceinline__ void block_tree(uint32_t nodes, uint32_t cnt, uint32_
             uint32_t l[8], r[8];
             load_node(nodes, 2 * tid, l);
             load_node(nodes, 2 * tid + 1, r);
-            parent(key, l, r, false, res);
+            parent(key, mode_flags, l, r, false, res);
             have = true;
         } else if (tid == half && (cnt & 1u)) {
             load_node(nodes, cnt - 1, res);
@@ -443,7 +446,7 @@ __device__ __forceinline__ void block_tree(uint32_t nodes, uint32_t cnt, uint32_
         if (tid < cnt) load_node(nodes, tid, out);
     }
     named_bar_sync(bar_id, nthreads);  // the node buffer is free again
-    if (tid < 32) warp_tree(out, cnt, key, root);
+    if (tid < 32) warp_tree(out, cnt, key, mode_flags, root);
 }
 
 }  // namespace b3g

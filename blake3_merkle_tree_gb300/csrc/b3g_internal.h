@@ -19,7 +19,22 @@ constexpr int kMaxGroupLog2 = 10;
 constexpr int kDefaultGroupLog2 = 10;
 // Default limit of every device-side wait: far above any real wait (microseconds),
 // far below a hang.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitLimitNs = 2000000000u;
+
+// Hash modes (page section "BLAKE3": the initial chaining value is an IV by default,
+// the user's key in keyed mode).  A mode is its initial CV (the key words, or the IV)
+// and the flag bits every one of its compressions carries.
+constexpr uint32_t kModeKeyed = 16u;   // KEYED_HASH
+constexpr uint32_t kModeDefault = 0u;  // no mode bit
+constexpr uint32_t kIvWords[8] = {0x6A09E667u, 0xBB67AE85u, 0x3C6EF372u, 0xA54FF53Au,
+                                  0x510E527Fu, 0x9B05688Cu, 0x1F83D9ABu, 0x5BE0CD19u};
+
+// The IV as 32 little-endian key bytes: the default mode runs the keyed machinery
+// with these as its key and kModeDefault as its flag bits.
+inline void iv_key_bytes(uint8_t out[32]) {
+    for (int i = 0; i < 8; ++i)
+        for (int b = 0; b < 4; ++b) out[4 * i + b] = static_cast<uint8_t>(kIvWords[i] >> (8 * b));
+}
 
 // Arguments of the leaf kernels (page section "Kernel 1": every CTA compresses a
 // group of 2^t chunks and reduces them to one subtree CV).
@@ -32,8 +47,9 @@ struct LeafArgs {
     uint64_t n_tiles;       // ceil(n_chunks / 2^t)
     uint8_t *out;           // tile CVs (32 B each) or chunk CVs (32 B each)
     uint32_t *status;       // device status word
-    uint64_t wait_limit_ns;
-    uint32_t key[8];
+    uint32_t wait_limit_ns; // limit of every device-side wait (at most 4.29 s)
+    uint32_t mode_flags;    // flag bits of the hash mode on every compression
+    uint32_t key[8];        // initial CV of every chunk and parent (the key, or the IV)
     uint32_t root;        // ROOT on the final compression if the whole tree is one tile
     uint32_t tail_bytes;  // bytes of the partial last chunk; 0 if none
     // Fused final reduction (at most 32 tiles): when `ticket` is not NULL (a zeroed
@@ -52,6 +68,7 @@ struct ReduceArgs {
     uint64_t count;
     uint8_t *out;       // ceil(count / group) CVs
     uint32_t key[8];
+    uint32_t mode_flags;
     uint32_t root;      // ROOT on the final compression when one group remains
     uint32_t group;     // CVs per CTA, a power of two in 2..1024
 };
@@ -98,7 +115,12 @@ b3g_status device_status_word(uint32_t **out);
 // The CV of the subtree made of the chunks of d_in[0..len) whose first chunk has global
 // index chunk_offset (ROOT on the final compression if root), written to d_out32;
 // ws holds blake3_workspace_size(len) bytes.
-b3g_status hash_range_ws(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32], bool root,
-                         uint8_t *d_out32, uint8_t *ws, cudaStream_t stream);
+b3g_status hash_range_ws(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
+                         uint32_t mode_flags, bool root, uint8_t *d_out32, uint8_t *ws, cudaStream_t stream);
+
+// Reduction of `count` CVs (a perfect or right-folded subtree) to d_out32 with groups of
+// 2^kDefaultGroupLog2; ws holds blake3_reduce_workspace_size(count, -1) bytes.
+b3g_status reduce_cvs_ws(const uint8_t *d_cvs, uint64_t count, const uint32_t key[8], uint32_t mode_flags,
+                         bool root, uint8_t *d_out32, uint8_t *ws, size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace b3g

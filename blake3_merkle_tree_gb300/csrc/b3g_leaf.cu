@@ -144,15 +144,18 @@ struct Words8 {
 // read straight from global memory with bounds checks.  Only the one thread that owns
 // that chunk calls it, once, so it is kept out of line, away from the hot loop; all
 // arguments and the result travel by value so that no caller array escapes.
+// `last_flags` is the flag word of the chunk's last block: the mode bits with
+// CHUNK_END (and ROOT); the blocks before it carry the mode bits alone.
 __device__ __noinline__ Words8 partial_chunk_cv(const uint8_t *in, uint64_t len, uint64_t off, uint64_t ctr,
-                                                uint32_t bytes, uint32_t end_flags, Words8 key) {
+                                                uint32_t bytes, uint32_t last_flags, Words8 key) {
     const uint32_t nblocks = (bytes + 63u) / 64u;
+    const uint32_t mode_flags = last_flags & ~(kChunkEnd | kRoot);
     Words8 cv = key;
     for (uint32_t b = 0; b < nblocks; ++b) {
         uint32_t m[16];
         load_block_global(in, len, off + 64ull * b, m);
         const bool last = b + 1 == nblocks;
-        const uint32_t flags = kKeyedHash | (b == 0 ? kChunkStart : 0u) | (last ? end_flags : 0u);
+        const uint32_t flags = (last ? last_flags : mode_flags) | (b == 0 ? kChunkStart : 0u);
         compress(cv.w, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32),
                  last ? bytes - 64u * (nblocks - 1u) : 64u, flags);
     }
@@ -161,13 +164,13 @@ __device__ __noinline__ Words8 partial_chunk_cv(const uint8_t *in, uint64_t len,
 
 // One tree level in shared memory: node j of `dst` = parent(node 2j, node 2j+1 of
 // `src`) for j < half, the lanes of the calling warp striding over j.
-__device__ B3G_PAIR_ATTR void pair_level(uint32_t src, uint32_t dst, uint32_t half, Words8 key) {
+__device__ B3G_PAIR_ATTR void pair_level(uint32_t src, uint32_t dst, uint32_t half, Words8 key, uint32_t mode_flags) {
     const uint32_t lane = threadIdx.x & 31u;
     for (uint32_t j = lane; j < half; j += 32) {
         uint32_t l[8], r[8], p[8];
         load_node(src, 2 * j, l);
         load_node(src, 2 * j + 1, r);
-        parent(key.w, l, r, false, p);
+        parent(key.w, mode_flags, l, r, false, p);
         store_node(dst, j, p);
     }
 }
@@ -177,7 +180,7 @@ __device__ B3G_PAIR_ATTR void pair_level(uint32_t src, uint32_t dst, uint32_t ha
 // last ticket has seen every other tile CV published (each is stored, then fenced,
 // before its warp takes a ticket) and folds them with the warp-level tree, ROOT on
 // the final compression.  This replaces the separate reduction launch for small inputs.
-__device__ __forceinline__ void fused_final_reduce(const LeafArgs &a, const uint32_t key[8]) {
+__device__ __forceinline__ void fused_final_reduce(const LeafArgs &a, const uint32_t key[8], uint32_t mode_flags) {
     const uint32_t lane = threadIdx.x & 31u;
     uint32_t ticket = 0;
     if (lane == 0) {
@@ -195,7 +198,7 @@ __device__ __forceinline__ void fused_final_reduce(const LeafArgs &a, const uint
         x[0] = w0.x; x[1] = w0.y; x[2] = w0.z; x[3] = w0.w;
         x[4] = w1.x; x[5] = w1.y; x[6] = w1.z; x[7] = w1.w;
     }
-    warp_tree(x, n, key, a.root != 0);
+    warp_tree(x, n, key, mode_flags, a.root != 0);
     if (lane == 0) {
         uint4 *o = reinterpret_cast<uint4 *>(a.final_out);
         o[0] = make_uint4(x[0], x[1], x[2], x[3]);
@@ -203,7 +206,7 @@ __device__ __forceinline__ void fused_final_reduce(const LeafArgs &a, const uint
     }
 }
 
-template <int C, int S, int LOAD, bool CHUNK_CVS>
+template <int C, int S, int LOAD, bool CHUNK_CVS, uint32_t MODE>
 __global__ void B3G_LEAF_BOUNDS(C + 32)
     leaf_tma_kernel(const __grid_constant__ CUtensorMap tmap, const LeafArgs a) {
     using Cfg = TmaCfg<C, S, LOAD, CHUNK_CVS>;
@@ -259,7 +262,7 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
                 if (pending == 0) return;
                 uint32_t n = pending * 32u, src = topA, dst = topB;
                 while (n > pending) {
-                    pair_level(src, dst, n >> 1, key8);
+                    pair_level(src, dst, n >> 1, key8, MODE);
                     __syncwarp();
                     const uint32_t t = src;
                     src = dst;
@@ -292,7 +295,7 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
                     uint32_t src = src0, level = 0;
                     for (uint32_t n = C; n > 32; n >>= 1, ++level) {
                         const uint32_t dst = n == 64 ? slot : ((level & 1u) ? scratch2 : scratch1);
-                        pair_level(src, dst, n >> 1, key8);
+                        pair_level(src, dst, n >> 1, key8, MODE);
                         __syncwarp();
                         if (level == 0) mbar_arrive(cvempty0 + 8 * b);  // node buffer read
                         src = dst;
@@ -319,7 +322,7 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
                 while (cnt > 32) {
                     const uint32_t dst = (level & 1u) ? scratch2 : scratch1;
                     const uint32_t half = cnt >> 1;
-                    pair_level(src, dst, half, key8);
+                    pair_level(src, dst, half, key8, MODE);
                     if ((cnt & 1u) && lane == 0) {
                         uint32_t t[8];
                         load_node(src, cnt - 1, t);
@@ -335,13 +338,13 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
                 if (lane < cnt) load_node(src, lane, x);
                 __syncwarp();
                 if (level == 0) mbar_arrive(cvempty0 + 8 * b);
-                warp_tree(x, cnt, key, a.root && a.n_tiles == 1);
+                warp_tree(x, cnt, key, MODE, a.root && a.n_tiles == 1);
                 if (lane == 0) {
                     uint4 *o = reinterpret_cast<uint4 *>(a.out + tile * 32);
                     o[0] = make_uint4(x[0], x[1], x[2], x[3]);
                     o[1] = make_uint4(x[4], x[5], x[6], x[7]);
                 }
-                if (a.ticket) fused_final_reduce(a, key);
+                if (a.ticket) fused_final_reduce(a, key, MODE);
             }
             flush();
         }
@@ -406,7 +409,7 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
         uint32_t cv[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) cv[i] = key[i];
-        uint32_t flags = kKeyedHash | kChunkStart;
+        uint32_t flags = MODE | kChunkStart;
 
 #pragma unroll kCopyLoopUnroll
         for (int ld = 0; ld < Cfg::kLoadsPerChunk; ++ld) {
@@ -431,7 +434,7 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
                     m[4 * q + 3] = w.w;
                 }
                 compress(cv, m, ctr_lo, ctr_hi, 64u, b == 15 ? (flags | end_flags) : flags);
-                flags = kKeyedHash;
+                flags = MODE;
             }
             // every lane has consumed stage st (its words went into the compression):
             // refill it with the copy S positions ahead
@@ -451,7 +454,7 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
             Words8 k8, t;
 #pragma unroll
             for (int i = 0; i < 8; ++i) k8.w[i] = key[i];
-            t = partial_chunk_cv(a.in, a.len, chunk * kChunkBytes, ctr, a.tail_bytes, end_flags, k8);
+            t = partial_chunk_cv(a.in, a.len, chunk * kChunkBytes, ctr, a.tail_bytes, MODE | end_flags, k8);
 #pragma unroll
             for (int i = 0; i < 8; ++i) cv[i] = t.w[i];
         }
@@ -491,7 +494,7 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
 // full chunk).  Same tiles and subtree as the TMA kernel; each thread reads its
 // chunk's blocks from global memory with bounds checks.
 // ---------------------------------------------------------------------------------
-template <int C, bool CHUNK_CVS>
+template <int C, bool CHUNK_CVS, uint32_t MODE>
 __global__ void __launch_bounds__(C) leaf_direct_kernel(const LeafArgs a) {
     __shared__ __align__(128) uint8_t node_mem[C * 32];
     const uint32_t nodes = smem_u32(node_mem);
@@ -521,7 +524,7 @@ __global__ void __launch_bounds__(C) leaf_direct_kernel(const LeafArgs a) {
                 uint32_t m[16];
                 load_block_global(a.in, a.len, start + 64ull * b, m);
                 const bool last = b + 1 == nblocks;
-                const uint32_t flags = kKeyedHash | (b == 0 ? kChunkStart : 0u) | (last ? end_flags : 0u);
+                const uint32_t flags = MODE | (b == 0 ? kChunkStart : 0u) | (last ? end_flags : 0u);
                 compress(cv, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32),
                          last ? last_len : 64u, flags);
             }
@@ -538,7 +541,7 @@ __global__ void __launch_bounds__(C) leaf_direct_kernel(const LeafArgs a) {
             const uint64_t rem = a.n_chunks - tile * C;
             const uint32_t cnt = rem < C ? static_cast<uint32_t>(rem) : static_cast<uint32_t>(C);
             uint32_t root_cv[8];
-            block_tree(nodes, cnt, r, C, kBarTree, key, a.root && a.n_tiles == 1, root_cv);
+            block_tree(nodes, cnt, r, C, kBarTree, key, MODE, a.root && a.n_tiles == 1, root_cv);
             if (r == 0) {
                 uint4 *o = reinterpret_cast<uint4 *>(a.out + tile * 32);
                 o[0] = make_uint4(root_cv[0], root_cv[1], root_cv[2], root_cv[3]);
@@ -657,11 +660,11 @@ uint64_t grid_for(uint64_t n_tiles, int blocks_per_sm, int sms) {
     return n_tiles < cap ? n_tiles : cap;
 }
 
-template <int C, bool CV>
+template <int C, bool CV, uint32_t MODE>
 b3g_status launch_tma(const LeafArgs &a, cudaStream_t stream, int dev, const DeviceInfo &info) {
     using T = Tuning<C>;
     using Cfg = TmaCfg<C, T::S, T::LOAD, CV>;
-    auto kernel = leaf_tma_kernel<C, T::S, T::LOAD, CV>;
+    auto kernel = leaf_tma_kernel<C, T::S, T::LOAD, CV, MODE>;
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
     if (!encode) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled unavailable");
     CUtensorMap tmap;
@@ -685,9 +688,9 @@ b3g_status launch_tma(const LeafArgs &a, cudaStream_t stream, int dev, const Dev
     return e == cudaSuccess ? B3G_OK : cuda_fail(e, "leaf_tma_kernel launch");
 }
 
-template <int C, bool CV>
+template <int C, bool CV, uint32_t MODE>
 b3g_status launch_direct(const LeafArgs &a, cudaStream_t stream, int dev, const DeviceInfo &info) {
-    auto kernel = leaf_direct_kernel<C, CV>;
+    auto kernel = leaf_direct_kernel<C, CV, MODE>;
     int bps = 0;
     b3g_status st = kernel_blocks_per_sm(reinterpret_cast<const void *>(kernel), C, 0, dev, bps);
     if (st != B3G_OK) return st;
@@ -696,11 +699,22 @@ b3g_status launch_direct(const LeafArgs &a, cudaStream_t stream, int dev, const 
     return e == cudaSuccess ? B3G_OK : cuda_fail(e, "leaf_direct_kernel launch");
 }
 
+// The hash mode is a template parameter of the kernels, so that the keyed kernels
+// compile exactly as without a mode; chunk CVs exist in keyed mode only.
 template <int C>
 b3g_status launch_c(const LeafArgs &a, bool chunk_cvs, bool tma, cudaStream_t stream, int dev,
                     const DeviceInfo &info) {
-    if (tma) return chunk_cvs ? launch_tma<C, true>(a, stream, dev, info) : launch_tma<C, false>(a, stream, dev, info);
-    return chunk_cvs ? launch_direct<C, true>(a, stream, dev, info) : launch_direct<C, false>(a, stream, dev, info);
+    if (a.mode_flags == kModeDefault) {
+        if (chunk_cvs) return B3G_ERR_ARG;
+        return tma ? launch_tma<C, false, kModeDefault>(a, stream, dev, info)
+                   : launch_direct<C, false, kModeDefault>(a, stream, dev, info);
+    }
+    if (a.mode_flags != kModeKeyed) return B3G_ERR_ARG;
+    if (tma)
+        return chunk_cvs ? launch_tma<C, true, kModeKeyed>(a, stream, dev, info)
+                         : launch_tma<C, false, kModeKeyed>(a, stream, dev, info);
+    return chunk_cvs ? launch_direct<C, true, kModeKeyed>(a, stream, dev, info)
+                     : launch_direct<C, false, kModeKeyed>(a, stream, dev, info);
 }
 
 }  // namespace
@@ -711,7 +725,7 @@ const char *kernel_config() {
     std::call_once(once, [] {
         std::snprintf(buf, sizeof buf,
                       "leaf_tma_kernel<%d,%d,%d> unroll=%d min_blocks=%d g_form=%d top_batch=%d pair_noinline=%d "
-                      "rot_fma=0x%x pdl=1",
+                      "rot_fma=0x%x pdl=1 modes=2",
                       1 << kDefaultLeavesLog2, Tuning<(1 << kDefaultLeavesLog2)>::S,
                       Tuning<(1 << kDefaultLeavesLog2)>::LOAD, kCopyLoopUnroll, B3G_MIN_BLOCKS, B3G_G_FORM,
                       B3G_TOP_BATCH, B3G_PAIR_NOINLINE, static_cast<unsigned>(B3G_ROT_FMA));

@@ -102,6 +102,7 @@ extern "C" b3g_status blake3_keyed_hash_noalloc(const void *d_in, uint64_t len, 
     for (int i = 0; i < 8; ++i)
         a.key[i] = static_cast<uint32_t>(key[4 * i]) | (static_cast<uint32_t>(key[4 * i + 1]) << 8) |
                    (static_cast<uint32_t>(key[4 * i + 2]) << 16) | (static_cast<uint32_t>(key[4 * i + 3]) << 24);
+    a.mode_flags = kModeKeyed;
     a.root = 1;
     a.tail_bytes = static_cast<uint32_t>(len % kChunkBytes);
     a.ticket = nullptr;
@@ -126,6 +127,7 @@ extern "C" b3g_status blake3_keyed_hash_noalloc(const void *d_in, uint64_t len, 
         const uint64_t groups = ceil_div(c, group);
         ra.out = groups == 1 ? d_out32 : next;
         std::memcpy(ra.key, a.key, sizeof ra.key);
+        ra.mode_flags = kModeKeyed;
         ra.root = 1;
         ra.group = static_cast<uint32_t>(group);
         st = launch_reduce(ra, s);

@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kReduceMaxThreads) reduce_cvs_kernel(const Red
         uint4 w0 = p[0], w1 = p[1], w2 = p[2], w3 = p[3];
         uint32_t l[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         uint32_t r[8] = {w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
-        parent(key, l, r, final_group && m == 2, res);
+        parent(key, a.mode_flags, l, r, final_group && m == 2, res);
         have = true;
     } else if (tid == half && (m & 1u)) {
         const uint4 *p = reinterpret_cast<const uint4 *>(a.in + (first + m - 1) * 32);
@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kReduceMaxThreads) reduce_cvs_kernel(const Red
     if (have) store_node(nodes, tid, res);
     named_bar_sync(kBarReduce, nthreads);
     uint32_t out[8];
-    block_tree(nodes, (m + 1) >> 1, tid, nthreads, kBarReduce, key, final_group, out);
+    block_tree(nodes, (m + 1) >> 1, tid, nthreads, kBarReduce, key, a.mode_flags, final_group, out);
     if (tid == 0) {
         uint4 *o = reinterpret_cast<uint4 *>(a.out + static_cast<uint64_t>(blockIdx.x) * 32);
         o[0] = make_uint4(out[0], out[1], out[2], out[3]);

@@ -59,7 +59,7 @@ constexpr size_t kStateBytes = kRecordOff + 128;
 constexpr int kRecWords = 26;
 
 // Root record of one chunk of `len` (0..1024) bytes at `p`, with counter ctr.
-__device__ void chunk_record(const uint8_t *p, uint32_t len, uint64_t ctr, const uint32_t key[8],
+__device__ void chunk_record(const uint8_t *p, uint32_t len, uint64_t ctr, const uint32_t key[8], uint32_t mode_flags,
                              uint32_t *rec) {
     const uint32_t nblocks = len == 0 ? 1u : (len + 63u) / 64u;
     uint32_t cv[8];
@@ -68,21 +68,21 @@ __device__ void chunk_record(const uint8_t *p, uint32_t len, uint64_t ctr, const
     for (uint32_t b = 0; b + 1 < nblocks; ++b) {
         load_block_global(p, len, 64ull * b, m);
         compress(cv, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32), 64u,
-                 kKeyedHash | (b == 0 ? kChunkStart : 0u));
+                 mode_flags | (b == 0 ? kChunkStart : 0u));
     }
     const uint32_t b = nblocks - 1;
     load_block_global(p, len, 64ull * b, m);
     for (int i = 0; i < 8; ++i) rec[i] = cv[i];
     for (int i = 0; i < 16; ++i) rec[8 + i] = m[i];
     rec[24] = len - 64u * b;
-    rec[25] = kKeyedHash | kChunkEnd | (b == 0 ? kChunkStart : 0u);
+    rec[25] = mode_flags | kChunkEnd | (b == 0 ? kChunkStart : 0u);
 }
 
 // CV (no ROOT) of one chunk.
-__device__ void chunk_cv(const uint8_t *p, uint32_t len, uint64_t ctr, const uint32_t key[8],
+__device__ void chunk_cv(const uint8_t *p, uint32_t len, uint64_t ctr, const uint32_t key[8], uint32_t mode_flags,
                          uint32_t cv[8]) {
     uint32_t r[kRecWords];
-    chunk_record(p, len, ctr, key, r);
+    chunk_record(p, len, ctr, key, mode_flags, r);
     uint32_t m[16];
     for (int i = 0; i < 8; ++i) cv[i] = r[i];
     for (int i = 0; i < 16; ++i) m[i] = r[8 + i];
@@ -90,14 +90,15 @@ __device__ void chunk_cv(const uint8_t *p, uint32_t len, uint64_t ctr, const uin
 }
 
 // Merge the top of a stack of CVs (8 words each) down to `target` entries.
-__device__ uint32_t merge_down(uint32_t *st, uint32_t depth, uint32_t target, const uint32_t key[8]) {
+__device__ uint32_t merge_down(uint32_t *st, uint32_t depth, uint32_t target, const uint32_t key[8],
+                               uint32_t mode_flags) {
     while (depth > target) {
         uint32_t l[8], r[8], p[8];
         for (int i = 0; i < 8; ++i) {
             l[i] = st[8 * (depth - 2) + i];
             r[i] = st[8 * (depth - 1) + i];
         }
-        parent(key, l, r, false, p);
+        parent(key, mode_flags, l, r, false, p);
         for (int i = 0; i < 8; ++i) st[8 * (depth - 2) + i] = p[i];
         --depth;
     }
@@ -124,7 +125,8 @@ struct RecordArgs {
     uint32_t depth;     // stack entries
     uint32_t target;    // stack entries after merging (kRecPush, kRecMerge)
     uint32_t mode;
-    uint32_t key[8];
+    uint32_t key[8];      // the key, or the IV in the default mode
+    uint32_t mode_flags;  // flag bits of the hash mode on every compression
     // kRecPushMany: roots of `npieces` pieces (32 bytes each) and their chunk positions
     const uint8_t *roots;
     uint32_t npieces;
@@ -141,22 +143,22 @@ __global__ void record_kernel(const RecordArgs a) {
     uint32_t *rec = reinterpret_cast<uint32_t *>(a.state + kRecordOff);
     switch (a.mode) {
         case kRecChunk:
-            chunk_record(a.in, a.len, a.pushed, key, rec);
+            chunk_record(a.in, a.len, a.pushed, key, a.mode_flags, rec);
             return;
         case kRecMerge:
-            merge_down(stack, a.depth, a.target, key);
+            merge_down(stack, a.depth, a.target, key, a.mode_flags);
             return;
         case kRecPush: {
-            const uint32_t d = merge_down(stack, a.depth, a.target, key);
+            const uint32_t d = merge_down(stack, a.depth, a.target, key, a.mode_flags);
             uint32_t cv[8];
-            chunk_cv(a.in, 1024u, a.pushed, key, cv);
+            chunk_cv(a.in, 1024u, a.pushed, key, a.mode_flags, cv);
             for (int i = 0; i < 8; ++i) stack[8 * d + i] = cv[i];
             return;
         }
         case kRecPushMany: {
             uint32_t d = a.depth;
             for (uint32_t j = 0; j < a.npieces; ++j) {
-                d = merge_down(stack, d, static_cast<uint32_t>(__popcll(a.piece_pos[j])), key);
+                d = merge_down(stack, d, static_cast<uint32_t>(__popcll(a.piece_pos[j])), key, a.mode_flags);
                 const uint32_t *rw = reinterpret_cast<const uint32_t *>(a.roots + 32ull * j);
                 for (int i = 0; i < 8; ++i) stack[8 * d + i] = rw[i];
                 ++d;
@@ -166,7 +168,7 @@ __global__ void record_kernel(const RecordArgs a) {
         case kRecParent:
             for (int i = 0; i < 8; ++i) rec[i] = key[i];
             rec[24] = kBlockLen;
-            rec[25] = kKeyedHash | kParent;
+            rec[25] = a.mode_flags | kParent;
             return;
         case kRecFinalize: {
             uint32_t st[kStackSlots * 8];  // a private copy: the hasher state is not changed
@@ -174,19 +176,19 @@ __global__ void record_kernel(const RecordArgs a) {
             uint32_t d = a.depth;
             uint64_t n = a.pushed;
             if (a.len > 0) {  // the unfinished chunk becomes the last leaf
-                d = merge_down(st, d, static_cast<uint32_t>(__popcll(n)), key);
-                chunk_cv(a.in, a.len, n, key, st + 8 * d);
+                d = merge_down(st, d, static_cast<uint32_t>(__popcll(n)), key, a.mode_flags);
+                chunk_cv(a.in, a.len, n, key, a.mode_flags, st + 8 * d);
                 ++d;
                 ++n;
             }
             const uint32_t pc = static_cast<uint32_t>(__popcll(n));
-            d = merge_down(st, d, pc < 2 ? 2u : pc, key);
+            d = merge_down(st, d, pc < 2 ? 2u : pc, key, a.mode_flags);
             uint32_t cv[8];
             for (int i = 0; i < 8; ++i) cv[i] = st[8 * (d - 1) + i];
             for (uint32_t e = d - 1; e > 1; --e) {
                 uint32_t l[8];
                 for (int i = 0; i < 8; ++i) l[i] = st[8 * (e - 1) + i];
-                parent(key, l, cv, false, cv);
+                parent(key, a.mode_flags, l, cv, false, cv);
             }
             for (int i = 0; i < 8; ++i) {
                 rec[i] = key[i];
@@ -194,7 +196,7 @@ __global__ void record_kernel(const RecordArgs a) {
                 rec[16 + i] = cv[i];
             }
             rec[24] = kBlockLen;
-            rec[25] = kKeyedHash | kParent;
+            rec[25] = a.mode_flags | kParent;
             return;
         }
         default:
@@ -208,6 +210,7 @@ struct PiecesArgs {
     const uint8_t *base;  // piece j starts at base + off[j]
     uint8_t *out;         // root of piece j at out + 32 * slot[j]
     uint32_t key[8];
+    uint32_t mode_flags;
     uint64_t off[kMaxSmallPieces];
     uint64_t counter[kMaxSmallPieces];
     uint32_t nchunks[kMaxSmallPieces];
@@ -232,14 +235,14 @@ __global__ void __launch_bounds__(64) pieces_kernel(const PiecesArgs a) {
         for (uint32_t b = 0; b < 16; ++b) {
             uint32_t m[16];
             load_block_global(p, 1024, 64ull * b, m);
-            const uint32_t flags = kKeyedHash | (b == 0 ? kChunkStart : 0u) | (b == 15 ? kChunkEnd : 0u);
+            const uint32_t flags = a.mode_flags | (b == 0 ? kChunkStart : 0u) | (b == 15 ? kChunkEnd : 0u);
             compress(cv, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32), 64u, flags);
         }
         store_node(nodes, r, cv);
     }
     named_bar_sync(1, 64);
     uint32_t root[8];
-    block_tree(nodes, cnt, r, 64, 1, key, false, root);
+    block_tree(nodes, cnt, r, 64, 1, key, a.mode_flags, false, root);
     if (r == 0) {
         uint4 *o = reinterpret_cast<uint4 *>(a.out + 32ull * a.slot[j]);
         o[0] = make_uint4(root[0], root[1], root[2], root[3]);
@@ -253,6 +256,7 @@ struct RangesArgs {
     const uint8_t *in;
     uint8_t *out;
     uint32_t key[8];
+    uint32_t mode_flags;
     uint32_t start[kMaxPieces];
     uint32_t count[kMaxPieces];
     uint32_t slot[kMaxPieces];
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(512) ranges_reduce_kernel(const RangesArgs a) 
         uint32_t l[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         uint32_t r[8] = {w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
         uint32_t res[8];
-        parent(key, l, r, false, res);
+        parent(key, a.mode_flags, l, r, false, res);
         store_node(nodes, tid, res);
     } else if (m == 1 && tid == 0) {
         const uint4 *p = reinterpret_cast<const uint4 *>(in);
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(512) ranges_reduce_kernel(const RangesArgs a) 
     }
     named_bar_sync(1, blockDim.x);
     uint32_t root[8];
-    block_tree(nodes, m == 1 ? 1u : half, tid, blockDim.x, 1, key, false, root);
+    block_tree(nodes, m == 1 ? 1u : half, tid, blockDim.x, 1, key, a.mode_flags, false, root);
     if (tid == 0) {
         uint4 *o = reinterpret_cast<uint4 *>(a.out + 32ull * a.slot[j]);
         o[0] = make_uint4(root[0], root[1], root[2], root[3]);
@@ -351,11 +355,12 @@ void key_words(const uint8_t key[32], uint32_t out[8]) {
                  (static_cast<uint32_t>(key[4 * i + 2]) << 16) | (static_cast<uint32_t>(key[4 * i + 3]) << 24);
 }
 
-RecordArgs record_args(uint8_t *state, const uint32_t key[8], uint32_t mode) {
+RecordArgs record_args(uint8_t *state, const uint32_t key[8], uint32_t mode_flags, uint32_t mode) {
     RecordArgs ra;
     std::memset(&ra, 0, sizeof ra);
     ra.state = state;
     std::memcpy(ra.key, key, sizeof ra.key);
+    ra.mode_flags = mode_flags;
     ra.mode = mode;
     return ra;
 }
@@ -404,8 +409,9 @@ using namespace b3g;
 // records) runs on the high-priority side stream `aux`, ordered against the caller's
 // stream with events, so that it overlaps the leaf launches on the caller's stream.
 struct b3g_hasher {
-    uint8_t key[32];
+    uint8_t key[32];      // the key, or the IV (little-endian) in the default mode
     uint32_t kw[8];
+    uint32_t mode_flags;  // KEYED_HASH in keyed mode, none in the default mode
     uint8_t *state;     // device: stack, 1024-byte chunk buffer, root record
     uint8_t *acc;       // device: bytes absorbed but not pushed (the state's buffer or own)
     uint64_t acc_cap;   // capacity of acc: 1024, or kAccBytes once grown
@@ -532,7 +538,7 @@ b3g_status push_pieces_one_by_one(b3g_hasher *h, const uint8_t *p, const std::ve
     for (const Piece &pc : pieces) {
         const uint32_t target = popcount64(pc.pos);
         if (h->depth > target) {
-            RecordArgs ra = record_args(h->state, h->kw, kRecMerge);
+            RecordArgs ra = record_args(h->state, h->kw, h->mode_flags, kRecMerge);
             ra.depth = h->depth;
             ra.target = target;
             st = launch_record(ra, x);
@@ -543,7 +549,7 @@ b3g_status push_pieces_one_by_one(b3g_hasher *h, const uint8_t *p, const std::ve
             st = B3G_ERR_ARG;
             break;
         }
-        st = hash_range_ws(p + (pc.pos - base) * kChunkBytes, pc.size * kChunkBytes, pc.pos, h->key, false,
+        st = hash_range_ws(p + (pc.pos - base) * kChunkBytes, pc.size * kChunkBytes, pc.pos, h->key, h->mode_flags, false,
                            h->state + 32ull * h->depth, ws, x);
         if (st != B3G_OK) break;
         h->depth += 1;
@@ -561,7 +567,7 @@ b3g_status push_pieces_one_by_one(b3g_hasher *h, const uint8_t *p, const std::ve
 b3g_status push_one(b3g_hasher *h, const uint8_t *p, cudaStream_t s) {
     b3g_status st = fork_aux(h, s);
     if (st != B3G_OK) return st;
-    RecordArgs ra = record_args(h->state, h->kw, kRecPush);
+    RecordArgs ra = record_args(h->state, h->kw, h->mode_flags, kRecPush);
     ra.in = p;
     ra.depth = h->depth;
     ra.target = popcount64(h->pushed);
@@ -633,6 +639,7 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
         pa.base = p;
         pa.out = roots;
         std::memcpy(pa.key, h->kw, sizeof pa.key);
+        pa.mode_flags = h->mode_flags;
         for (size_t i = 0; i < small.size(); ++i) {
             const Piece &pc = pieces[small[i]];
             pa.off[i] = (pc.pos - base) * kChunkBytes;
@@ -659,6 +666,7 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
             a.status = status;
             a.wait_limit_ns = kWaitLimitNs;
             std::memcpy(a.key, h->kw, sizeof a.key);
+            a.mode_flags = h->mode_flags;
             st = launch_leaf(a, kDefaultLeavesLog2, false, s);
         }
         if (st == B3G_OK) st = fork_aux(h, s);  // the tile CVs are ready
@@ -667,13 +675,13 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
         ra.in = tile_cvs;
         ra.out = roots;
         std::memcpy(ra.key, h->kw, sizeof ra.key);
+        ra.mode_flags = h->mode_flags;
         uint32_t nr = 0, widest = 1;
         for (size_t j : big) {
             if (st != B3G_OK) break;
             const uint64_t t0 = (pieces[j].pos - A) / tile, t = pieces[j].size / tile;
             if (t > 1024) {  // a very large piece: the ordinary multi-level reduction
-                st = blake3_keyed_reduce_cvs(tile_cvs + 32 * t0, t, h->key, 0, 10, roots + 32 * j, huge, huge_ws,
-                                             reinterpret_cast<b3g_stream_t>(x));
+                st = reduce_cvs_ws(tile_cvs + 32 * t0, t, h->kw, h->mode_flags, false, roots + 32 * j, huge, huge_ws, x);
                 continue;
             }
             ra.start[nr] = static_cast<uint32_t>(t0);
@@ -690,7 +698,7 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
         }
     }
     if (st == B3G_OK) {
-        RecordArgs rec = record_args(h->state, h->kw, kRecPushMany);
+        RecordArgs rec = record_args(h->state, h->kw, h->mode_flags, kRecPushMany);
         rec.depth = h->depth;
         rec.roots = roots;
         rec.npieces = static_cast<uint32_t>(pieces.size());
@@ -750,12 +758,12 @@ void hasher_clear(b3g_hasher *h) {
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-b3g_status blake3_keyed_hash_xof(const void *d_in, uint64_t len, const uint8_t key[32], uint8_t *d_out,
-                                 uint64_t out_len, b3g_stream_t stream) {
-    if (!key || (!d_out && out_len > 0) || (!d_in && len > 0)) return B3G_ERR_NULL;
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+// Extendable output of d_in[0..len) in the mode given by `key` (the key, or the IV)
+// and `mode_flags`.
+b3g_status xof_range(const void *d_in, uint64_t len, const uint8_t key[32], uint32_t mode_flags, uint8_t *d_out,
+                     uint64_t out_len, cudaStream_t s) {
     uint32_t kw[8];
     key_words(key, kw);
     const uint64_t n = len == 0 ? 1 : ceil_div(len, kChunkBytes);
@@ -773,18 +781,18 @@ b3g_status blake3_keyed_hash_xof(const void *d_in, uint64_t len, const uint8_t k
     uint32_t *rec = reinterpret_cast<uint32_t *>(scratch + kRecordOff);
     b3g_status st;
     if (n == 1) {
-        RecordArgs ra = record_args(scratch, kw, kRecChunk);
+        RecordArgs ra = record_args(scratch, kw, mode_flags, kRecChunk);
         ra.in = static_cast<const uint8_t *>(d_in);
         ra.len = static_cast<uint32_t>(len);
         st = launch_record(ra, s);
     } else {
         // the root's children, written straight into the record's message words
-        st = hash_range_ws(d_in, left_bytes, 0, key, false, reinterpret_cast<uint8_t *>(rec + 8), scratch + off1,
-                           s);
+        st = hash_range_ws(d_in, left_bytes, 0, key, mode_flags, false, reinterpret_cast<uint8_t *>(rec + 8),
+                           scratch + off1, s);
         if (st == B3G_OK)
-            st = hash_range_ws(static_cast<const uint8_t *>(d_in) + left_bytes, len - left_bytes, left_n, key, false,
-                               reinterpret_cast<uint8_t *>(rec + 16), scratch + off2, s);
-        if (st == B3G_OK) st = launch_record(record_args(scratch, kw, kRecParent), s);
+            st = hash_range_ws(static_cast<const uint8_t *>(d_in) + left_bytes, len - left_bytes, left_n, key,
+                               mode_flags, false, reinterpret_cast<uint8_t *>(rec + 16), scratch + off2, s);
+        if (st == B3G_OK) st = launch_record(record_args(scratch, kw, mode_flags, kRecParent), s);
     }
     if (st == B3G_OK) st = launch_xof(rec, d_out, out_len, s);
     e = cudaFreeAsync(scratch, s);
@@ -792,20 +800,21 @@ b3g_status blake3_keyed_hash_xof(const void *d_in, uint64_t len, const uint8_t k
     return st;
 }
 
-b3g_status blake3_hasher_new(const uint8_t key[32], b3g_hasher **out) {
-    if (!key || !out) return B3G_ERR_NULL;
+// A new hasher in the mode given by `key` (the key, or the IV) and `mode_flags`.
+b3g_status hasher_create(const uint8_t key[32], uint32_t mode_flags, b3g_hasher **out) {
     *out = nullptr;
     b3g_hasher *h = new (std::nothrow) b3g_hasher;
     if (!h) return B3G_ERR_ARG;
     std::memcpy(h->key, key, 32);
     key_words(key, h->kw);
+    h->mode_flags = mode_flags;
     hasher_clear(h);
     h->state = nullptr;
     cudaError_t e = cudaGetDevice(&h->device);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void **>(&h->state), kStateBytes);
     if (e != cudaSuccess) {
         delete h;
-        return cuda_fail(e, "blake3_hasher_new");
+        return cuda_fail(e, "hasher state");
     }
     h->acc = h->state + kBufOff;
     h->acc_cap = kChunkBytes;
@@ -819,6 +828,118 @@ b3g_status blake3_hasher_new(const uint8_t key[32], b3g_hasher **out) {
     }
     *out = h;
     return B3G_OK;
+}
+
+// Digest of host bytes in the mode given by `key` (the key, or the IV) and
+// `mode_flags`: copies into two staging slots overlap the hashing of the other slot.
+b3g_status host_range(const void *h_in, uint64_t len, const uint8_t key[32], uint32_t mode_flags, uint8_t out32[32],
+                      void *d_staging, size_t staging_bytes, b3g_stream_t stream) {
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t cs = nullptr;
+    b3g_status st = cached_stream(0, &cs);
+    if (st != B3G_OK) return st;
+    constexpr size_t kSlotAlign = 1u << 20;
+    constexpr size_t kHead = (kStateBytes + 255) & ~size_t(255);  // hasher state + digest
+    if (d_staging && (reinterpret_cast<uintptr_t>(d_staging) & 255u)) return B3G_ERR_ALIGN;
+    if (d_staging && staging_bytes < kHead + 2 * kSlotAlign) return B3G_ERR_WORKSPACE;
+    bool own = false;
+    if (!d_staging) {
+        staging_bytes = kHead + 2 * (64u << 20);
+        cudaError_t e = cudaMallocAsync(&d_staging, staging_bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
+        own = true;
+    }
+    const size_t slot = ((staging_bytes - kHead) / 2) & ~(kSlotAlign - 1);
+    uint8_t *base = static_cast<uint8_t *>(d_staging);
+    uint8_t *slots[2] = {base + kHead, base + kHead + slot};
+
+    // a hasher whose state lives in the staging area; slot-sized segments bypass acc
+    b3g_hasher h;
+    std::memcpy(h.key, key, 32);
+    key_words(key, h.kw);
+    h.mode_flags = mode_flags;
+    hasher_clear(&h);
+    h.own_streams = h.read_pending = false;
+    h.aux = nullptr;
+    h.ev_fork = h.ev_read = h.ev_done = nullptr;
+    h.state = base;
+    h.acc = base + kBufOff;
+    h.acc_cap = kChunkBytes;
+    h.may_grow = false;
+    cudaError_t e = cudaGetDevice(&h.device);
+    if (e != cudaSuccess) st = cuda_fail(e, "cudaGetDevice");
+    if (st == B3G_OK) st = streams_init(&h, false);
+
+    cudaEvent_t ev[5] = {};
+    for (int i = 0; i < 5 && st == B3G_OK && e == cudaSuccess; ++i)
+        e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    cudaEvent_t start = ev[0], copied[2] = {ev[1], ev[2]}, consumed[2] = {ev[3], ev[4]};
+    if (st == B3G_OK && e == cudaSuccess) e = cudaEventRecord(start, s);  // staging is free from here on
+    if (st == B3G_OK && e == cudaSuccess) e = cudaStreamWaitEvent(cs, start, 0);
+    if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "event set-up");
+    const uint8_t *src = static_cast<const uint8_t *>(h_in);
+    uint64_t off = 0;
+    for (uint64_t i = 0; st == B3G_OK && off < len; ++i) {
+        const int b = static_cast<int>(i & 1);
+        const uint64_t n = len - off < slot ? len - off : slot;
+        if (i >= 2) e = cudaStreamWaitEvent(cs, consumed[b], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(slots[b], src + off, n, cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(copied[b], cs);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, copied[b], 0);
+        if (e != cudaSuccess) {
+            st = cuda_fail(e, "staging copy");
+            break;
+        }
+        st = blake3_hasher_update(&h, slots[b], n, stream);
+        if (st == B3G_OK && (e = cudaEventRecord(consumed[b], s)) != cudaSuccess) st = cuda_fail(e, "cudaEventRecord");
+        off += n;
+    }
+    uint8_t *d_digest = base + kStateBytes;  // 32 bytes between the state and the slots
+    if (st == B3G_OK) st = blake3_hasher_finalize(&h, d_digest, 32, stream);
+    if (st == B3G_OK && (e = cudaMemcpyAsync(out32, d_digest, 32, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        st = cuda_fail(e, "cudaMemcpyAsync(digest)");
+    if (h.aux && h.ev_done) join_all(&h, s);  // also after an error: nothing on the side stream outlives the staging
+    if (own) {
+        e = cudaFreeAsync(d_staging, s);
+        if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
+    }
+    e = cudaStreamSynchronize(s);
+    if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaStreamSynchronize");
+    for (cudaEvent_t x : ev)
+        if (x) cudaEventDestroy(x);
+    streams_release(&h);
+    return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+b3g_status blake3_keyed_hash_xof(const void *d_in, uint64_t len, const uint8_t key[32], uint8_t *d_out,
+                                 uint64_t out_len, b3g_stream_t stream) {
+    if (!key || (!d_out && out_len > 0) || (!d_in && len > 0)) return B3G_ERR_NULL;
+    return xof_range(d_in, len, key, kModeKeyed, d_out, out_len, reinterpret_cast<cudaStream_t>(stream));
+}
+
+b3g_status blake3_hash_xof(const void *d_in, uint64_t len, uint8_t *d_out, uint64_t out_len, b3g_stream_t stream) {
+    if ((!d_out && out_len > 0) || (!d_in && len > 0)) return B3G_ERR_NULL;
+    uint8_t iv[32];
+    iv_key_bytes(iv);
+    return xof_range(d_in, len, iv, kModeDefault, d_out, out_len, reinterpret_cast<cudaStream_t>(stream));
+}
+
+
+
+b3g_status blake3_hasher_new(const uint8_t key[32], b3g_hasher **out) {
+    if (!key || !out) return B3G_ERR_NULL;
+    return hasher_create(key, kModeKeyed, out);
+}
+
+b3g_status blake3_hasher_new_default(b3g_hasher **out) {
+    if (!out) return B3G_ERR_NULL;
+    uint8_t iv[32];
+    iv_key_bytes(iv);
+    return hasher_create(iv, kModeDefault, out);
 }
 
 void blake3_hasher_free(b3g_hasher *h) {
@@ -899,83 +1020,19 @@ b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b
     return B3G_OK;
 }
 
+
 b3g_status blake3_keyed_hash_host(const void *h_in, uint64_t len, const uint8_t key[32], uint8_t out32[32],
                                   void *d_staging, size_t staging_bytes, b3g_stream_t stream) {
     if (!key || !out32 || (!h_in && len > 0)) return B3G_ERR_NULL;
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaStream_t cs = nullptr;
-    b3g_status st = cached_stream(0, &cs);
-    if (st != B3G_OK) return st;
-    constexpr size_t kSlotAlign = 1u << 20;
-    constexpr size_t kHead = (kStateBytes + 255) & ~size_t(255);  // hasher state + digest
-    if (d_staging && (reinterpret_cast<uintptr_t>(d_staging) & 255u)) return B3G_ERR_ALIGN;
-    if (d_staging && staging_bytes < kHead + 2 * kSlotAlign) return B3G_ERR_WORKSPACE;
-    bool own = false;
-    if (!d_staging) {
-        staging_bytes = kHead + 2 * (64u << 20);
-        cudaError_t e = cudaMallocAsync(&d_staging, staging_bytes, s);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
-        own = true;
-    }
-    const size_t slot = ((staging_bytes - kHead) / 2) & ~(kSlotAlign - 1);
-    uint8_t *base = static_cast<uint8_t *>(d_staging);
-    uint8_t *slots[2] = {base + kHead, base + kHead + slot};
+    return host_range(h_in, len, key, kModeKeyed, out32, d_staging, staging_bytes, stream);
+}
 
-    // a hasher whose state lives in the staging area; slot-sized segments bypass acc
-    b3g_hasher h;
-    std::memcpy(h.key, key, 32);
-    key_words(key, h.kw);
-    hasher_clear(&h);
-    h.own_streams = h.read_pending = false;
-    h.aux = nullptr;
-    h.ev_fork = h.ev_read = h.ev_done = nullptr;
-    h.state = base;
-    h.acc = base + kBufOff;
-    h.acc_cap = kChunkBytes;
-    h.may_grow = false;
-    cudaError_t e = cudaGetDevice(&h.device);
-    if (e != cudaSuccess) st = cuda_fail(e, "cudaGetDevice");
-    if (st == B3G_OK) st = streams_init(&h, false);
-
-    cudaEvent_t ev[5] = {};
-    for (int i = 0; i < 5 && st == B3G_OK && e == cudaSuccess; ++i)
-        e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
-    cudaEvent_t start = ev[0], copied[2] = {ev[1], ev[2]}, consumed[2] = {ev[3], ev[4]};
-    if (st == B3G_OK && e == cudaSuccess) e = cudaEventRecord(start, s);  // staging is free from here on
-    if (st == B3G_OK && e == cudaSuccess) e = cudaStreamWaitEvent(cs, start, 0);
-    if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "event set-up");
-    const uint8_t *src = static_cast<const uint8_t *>(h_in);
-    uint64_t off = 0;
-    for (uint64_t i = 0; st == B3G_OK && off < len; ++i) {
-        const int b = static_cast<int>(i & 1);
-        const uint64_t n = len - off < slot ? len - off : slot;
-        if (i >= 2) e = cudaStreamWaitEvent(cs, consumed[b], 0);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(slots[b], src + off, n, cudaMemcpyHostToDevice, cs);
-        if (e == cudaSuccess) e = cudaEventRecord(copied[b], cs);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, copied[b], 0);
-        if (e != cudaSuccess) {
-            st = cuda_fail(e, "staging copy");
-            break;
-        }
-        st = blake3_hasher_update(&h, slots[b], n, stream);
-        if (st == B3G_OK && (e = cudaEventRecord(consumed[b], s)) != cudaSuccess) st = cuda_fail(e, "cudaEventRecord");
-        off += n;
-    }
-    uint8_t *d_digest = base + kStateBytes;  // 32 bytes between the state and the slots
-    if (st == B3G_OK) st = blake3_hasher_finalize(&h, d_digest, 32, stream);
-    if (st == B3G_OK && (e = cudaMemcpyAsync(out32, d_digest, 32, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-        st = cuda_fail(e, "cudaMemcpyAsync(digest)");
-    if (h.aux && h.ev_done) join_all(&h, s);  // also after an error: nothing on the side stream outlives the staging
-    if (own) {
-        e = cudaFreeAsync(d_staging, s);
-        if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
-    }
-    e = cudaStreamSynchronize(s);
-    if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaStreamSynchronize");
-    for (cudaEvent_t x : ev)
-        if (x) cudaEventDestroy(x);
-    streams_release(&h);
-    return st;
+b3g_status blake3_hash_host(const void *h_in, uint64_t len, uint8_t out32[32], void *d_staging,
+                            size_t staging_bytes, b3g_stream_t stream) {
+    if (!out32 || (!h_in && len > 0)) return B3G_ERR_NULL;
+    uint8_t iv[32];
+    iv_key_bytes(iv);
+    return host_range(h_in, len, iv, kModeDefault, out32, d_staging, staging_bytes, stream);
 }
 
 b3g_status blake3_hasher_finalize(const b3g_hasher *hc, uint8_t *d_out, uint64_t out_len, b3g_stream_t stream) {
@@ -989,7 +1046,7 @@ b3g_status blake3_hasher_finalize(const b3g_hasher *hc, uint8_t *d_out, uint64_t
     st = join_all(&t, s);
     if (st != B3G_OK) return st;
     if (t.count <= kChunkBytes) {
-        RecordArgs ra = record_args(t.state, t.kw, kRecChunk);
+        RecordArgs ra = record_args(t.state, t.kw, t.mode_flags, kRecChunk);
         ra.in = t.acc;
         ra.len = static_cast<uint32_t>(t.count);
         st = launch_record(ra, s);
@@ -1012,7 +1069,7 @@ b3g_status blake3_hasher_finalize(const b3g_hasher *hc, uint8_t *d_out, uint64_t
         if (st == B3G_OK) st = js;
     }
     if (st == B3G_OK) {
-        RecordArgs ra = record_args(t.state, t.kw, kRecFinalize);
+        RecordArgs ra = record_args(t.state, t.kw, t.mode_flags, kRecFinalize);
         ra.in = t.acc + k * kChunkBytes;
         ra.len = static_cast<uint32_t>(t.acc_len - k * kChunkBytes);
         ra.depth = t.depth;

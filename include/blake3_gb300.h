@@ -124,6 +124,18 @@ b3g_status blake3_keyed_hash_ws(const void *d_in, uint64_t len, const uint8_t ke
                                 b3g_stream_t stream);
 
 /*
+ * blake3_hash / blake3_hash_ws -- the digest in the default (unkeyed) mode.  Page
+ * section "BLAKE3": a chunk's first block starts from an IV by default and from the
+ * user's key in keyed mode.  Here every chunk and every parent starts from the IV and
+ * no compression carries KEYED_HASH (the specification's hash mode); the kernels,
+ * tree, workspace size (blake3_workspace_size), alignment rules and errors are those
+ * of blake3_keyed_hash / blake3_keyed_hash_ws, without the key argument.
+ */
+b3g_status blake3_hash(const void *d_in, uint64_t len, uint8_t *d_out32, b3g_stream_t stream);
+b3g_status blake3_hash_ws(const void *d_in, uint64_t len, uint8_t *d_out32, void *d_ws, size_t ws_bytes,
+                          b3g_stream_t stream);
+
+/*
  * blake3_keyed_chunk_cvs -- the CV of every chunk of d_in[0..len), none with ROOT,
  * chunk i using counter chunk_offset + i (page section "压缩函数": one thread per
  * chunk, 16 chained block compressions).  d_cvs receives max(1, ceil(len/1024))
@@ -213,6 +225,11 @@ b3g_status blake3_selftest_bounded_wait(uint32_t limit_us, int *timed_out_out);
 b3g_status blake3_keyed_hash_xof(const void *d_in, uint64_t len, const uint8_t key[32],
                                  uint8_t *d_out, uint64_t out_len, b3g_stream_t stream);
 
+/* blake3_hash_xof -- extendable output in the default (unkeyed) mode; otherwise as
+ * blake3_keyed_hash_xof. */
+b3g_status blake3_hash_xof(const void *d_in, uint64_t len, uint8_t *d_out, uint64_t out_len,
+                           b3g_stream_t stream);
+
 /*
  * Streaming hasher: the digest of input that arrives as successive device segments of
  * any length, equal to the digest of their concatenation.  The hasher is a host object
@@ -235,6 +252,10 @@ typedef struct b3g_hasher b3g_hasher;
 /* Creates a hasher for `key` (host pointer, copied).  Allocates with cudaMalloc and
  * creates its side stream and events. */
 b3g_status blake3_hasher_new(const uint8_t key[32], b3g_hasher **out);
+
+/* Creates a hasher in the default (unkeyed) mode (see blake3_hash); otherwise as
+ * blake3_hasher_new. */
+b3g_status blake3_hasher_new_default(b3g_hasher **out);
 
 /* Frees the hasher, its device memory, stream and events (waits for its side stream;
  * cudaFree synchronises the device). */
@@ -269,6 +290,11 @@ b3g_status blake3_hasher_finalize(const b3g_hasher *h, uint8_t *d_out, uint64_t 
 b3g_status blake3_keyed_hash_host(const void *h_in, uint64_t len, const uint8_t key[32],
                                   uint8_t out32[32], void *d_staging, size_t staging_bytes,
                                   b3g_stream_t stream);
+
+/* blake3_hash_host -- the default-mode (unkeyed) digest of host memory; otherwise as
+ * blake3_keyed_hash_host. */
+b3g_status blake3_hash_host(const void *h_in, uint64_t len, uint8_t out32[32], void *d_staging,
+                            size_t staging_bytes, b3g_stream_t stream);
 
 /*
  * blake3_keyed_hash_noalloc -- the same digest as blake3_keyed_hash, computed without

@@ -5,7 +5,8 @@
  * Generates LEN bytes (byte i = (131 i + 7 (i >> 8) + 3) mod 256) and the key
  * (byte i = 7 i + 1), then prints one line of hex each for: blake3_keyed_hash, the
  * streaming hasher fed in three segments, 100 bytes of extendable output,
- * blake3_keyed_hash_host from pageable host memory, and the device status word.
+ * blake3_keyed_hash_host from pageable host memory, the default-mode digest
+ * (blake3_hash) and the device status word.
  * Exit status 0 on success, 1 with a message on stderr otherwise. */
 #include <stdint.h>
 #include <stdio.h>
@@ -73,6 +74,11 @@ int main(int argc, char **argv) {
 
     /* from pageable host memory, library-allocated staging */
     if (check(blake3_keyed_hash_host(host, len, key, out, NULL, 0, NULL), "blake3_keyed_hash_host")) return 1;
+    print_hex(out, 32);
+
+    /* default (unkeyed) mode */
+    if (check(blake3_hash(d_in, len, d_out, NULL), "blake3_hash")) return 1;
+    if (cudaMemcpy(out, d_out, 32, cudaMemcpyDeviceToHost) != cudaSuccess) return 1;
     print_hex(out, 32);
 
     uint32_t status = 0;

@@ -131,6 +131,24 @@ def test_host_entry_argument_errors(lib):
     assert lib.blake3_keyed_hash_host(None, 10, KEY, out, None, 0, None) == 1
 
 
+def test_default_mode_argument_errors(lib):
+    out = ctypes.create_string_buffer(32)
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.blake3_hash(None, 10, FAKE, None) == 1
+    assert lib.blake3_hash(FAKE, 10, None, None) == 1
+    assert lib.blake3_hash(FAKE, 10, odd, None) == 2
+    assert lib.blake3_hash_ws(FAKE, 1 << 30, FAKE, None, 0, None) == 3
+    assert lib.blake3_hash_ws(FAKE, 1 << 30, FAKE, ctypes.c_void_p(0x10001), 1 << 20, None) == 2
+    assert lib.blake3_hash_ws(FAKE, 10, odd, None, 0, None) == 2
+    assert lib.blake3_hash_xof(None, 10, FAKE, 32, None) == 1
+    assert lib.blake3_hash_xof(FAKE, 10, None, 32, None) == 1
+    assert lib.blake3_hasher_new_default(None) == 1
+    assert lib.blake3_hash_host(None, 10, out, None, 0, None) == 1
+    assert lib.blake3_hash_host(FAKE, 10, None, None, 0, None) == 1
+    # the workspace of the default mode is the keyed mode's
+    assert lib.blake3_workspace_size(1 << 30) > 0
+
+
 def test_options_and_config(lib):
     assert lib.blake3_set_option(99, 1) == 6
     assert lib.blake3_set_option(1, 0) == 0

@@ -41,11 +41,12 @@ def _inputs(n):
 def test_c_client_matches_oracle(client, n):
     p = subprocess.run([client, str(n)], capture_output=True, text=True, timeout=300)
     assert p.returncode == 0, p.stderr
-    one_shot, streamed, xof, from_host, status = p.stdout.split()
+    one_shot, streamed, xof, from_host, default_mode, status = p.stdout.split()
     data, key = _inputs(n)
     ref = oracle.keyed_hash(data, key).hex()
     assert one_shot == ref
     assert streamed == ref
     assert from_host == ref
     assert xof == oracle.keyed_hash_xof(data, key, 100).hex()
+    assert default_mode == oracle.hash(data).hex()
     assert status == "0"
