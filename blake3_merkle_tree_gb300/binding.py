@@ -69,6 +69,7 @@ def library() -> ctypes.CDLL:
             "blake3_hasher_reset": (i32, [vp]),
             "blake3_hasher_count": (u64, [vp]),
             "blake3_hasher_update": (i32, [vp, vp, u64, vp]),
+            "blake3_hasher_update_many": (i32, [vp, vp, vp, u64, vp]),
             "blake3_hasher_finalize": (i32, [vp, vp, u64, vp]),
             "blake3_keyed_hash_host": (i32, [vp, u64, vp, vp, vp, sz, vp]),
             "blake3_hash": (i32, [vp, u64, vp, vp]),
@@ -302,6 +303,17 @@ class Hasher:
     def update(self, data: torch.Tensor, stream=None) -> "Hasher":
         _check(library().blake3_hasher_update(self._h, _dev_ptr(data, "data"), _nbytes(data), _stream(stream)),
                "blake3_hasher_update")
+        return self
+
+    def update_many(self, segments, stream=None) -> "Hasher":
+        """Absorb a sequence of contiguous CUDA tensors in order, as one call (runs of small
+        segments are copied by one gather launch)."""
+        segs = list(segments)
+        n = len(segs)
+        ptrs = (ctypes.c_void_p * max(1, n))(*[_dev_ptr(t, "segment") for t in segs])
+        lens = (ctypes.c_uint64 * max(1, n))(*[_nbytes(t) for t in segs])
+        _check(library().blake3_hasher_update_many(self._h, ptrs, lens, n, _stream(stream)),
+               "blake3_hasher_update_many")
         return self
 
     def finalize(self, out_len: int = 32, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -296,6 +296,53 @@ __global__ void __launch_bounds__(512) ranges_reduce_kernel(const RangesArgs a) 
     }
 }
 
+// Gather copy for blake3_hasher_update_many: segment j (src[j], len[j] bytes) goes to
+// dst + off[j]; the copy is cut into pieces of kGatherPiece bytes, piece0[j] being
+// segment j's first piece, and CTA i copies piece i.  A piece whose source and
+// destination share their alignment modulo 16 moves 16-byte words between a byte head
+// and a byte tail; any other piece moves bytes.
+constexpr int kGatherMax = 128;
+constexpr uint32_t kGatherPiece = 32 * 1024;
+
+struct GatherArgs {
+    uint8_t *dst;
+    uint32_t n;
+    const uint8_t *src[kGatherMax];
+    uint64_t off[kGatherMax];
+    uint64_t len[kGatherMax];
+    uint32_t piece0[kGatherMax + 1];
+};
+
+__global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
+    const uint32_t piece = blockIdx.x;
+    uint32_t lo = 0, hi = a.n;  // the segment j with piece0[j] <= piece < piece0[j + 1]
+    while (hi - lo > 1) {
+        const uint32_t mid = (lo + hi) / 2;
+        if (a.piece0[mid] <= piece) lo = mid;
+        else hi = mid;
+    }
+    const uint32_t j = lo;
+    const uint64_t p0 = static_cast<uint64_t>(piece - a.piece0[j]) * kGatherPiece;
+    const uint64_t p1 = a.len[j] - p0 < kGatherPiece ? a.len[j] : p0 + kGatherPiece;
+    const uint8_t *src = a.src[j];
+    uint8_t *dst = a.dst + a.off[j];
+    const uint32_t t = threadIdx.x, nt = blockDim.x;
+    const uintptr_t sa = reinterpret_cast<uintptr_t>(src + p0), da = reinterpret_cast<uintptr_t>(dst + p0);
+    if ((sa & 15u) == (da & 15u)) {
+        uint64_t head = (16u - (sa & 15u)) & 15u;
+        head = head < p1 - p0 ? head : p1 - p0;
+        for (uint64_t i = t; i < head; i += nt) dst[p0 + i] = src[p0 + i];
+        const uint64_t q0 = p0 + head;
+        const uint64_t nvec = (p1 - q0) / 16;
+        const uint4 *sv = reinterpret_cast<const uint4 *>(src + q0);
+        uint4 *dv = reinterpret_cast<uint4 *>(dst + q0);
+        for (uint64_t i = t; i < nvec; i += nt) dv[i] = sv[i];
+        for (uint64_t i = q0 + 16 * nvec + t; i < p1; i += nt) dst[i] = src[i];
+    } else {
+        for (uint64_t i = p0 + t; i < p1; i += nt) dst[i] = src[i];
+    }
+}
+
 struct XofArgs {
     const uint32_t *rec;  // root record (device)
     uint8_t *out;
@@ -1020,6 +1067,62 @@ b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b
     return B3G_OK;
 }
 
+
+b3g_status blake3_hasher_update_many(b3g_hasher *h, const void *const *d_ptrs, const uint64_t *lens, uint64_t count,
+                                     b3g_stream_t stream) {
+    if (!h || (count > 0 && (!d_ptrs || !lens))) return B3G_ERR_NULL;
+    for (uint64_t i = 0; i < count; ++i)
+        if (!d_ptrs[i] && lens[i] > 0) return B3G_ERR_NULL;
+    if (count == 0) return B3G_OK;
+    b3g_status st = check_device(h->device);
+    if (st != B3G_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    uint64_t i = 0;
+    while (i < count) {
+        if (lens[i] == 0) {
+            ++i;
+            continue;
+        }
+        if (h->acc_len + lens[i] > h->acc_cap && h->may_grow && cap == cudaStreamCaptureStatusNone &&
+            lens[i] < kAccBytes) {
+            st = grow_acc(h, s);
+            if (st != B3G_OK) return st;
+        }
+        // the run of segments that fit in the accumulation buffer: one gather launch
+        GatherArgs ga;
+        ga.dst = h->acc + h->acc_len;
+        ga.n = 0;
+        uint64_t bytes = 0, pieces = 0;
+        while (i < count && ga.n < static_cast<uint32_t>(kGatherMax) && h->acc_len + bytes + lens[i] <= h->acc_cap) {
+            if (lens[i] > 0) {
+                ga.src[ga.n] = static_cast<const uint8_t *>(d_ptrs[i]);
+                ga.off[ga.n] = bytes;
+                ga.len[ga.n] = lens[i];
+                ga.piece0[ga.n] = static_cast<uint32_t>(pieces);
+                pieces += (lens[i] + kGatherPiece - 1) / kGatherPiece;
+                bytes += lens[i];
+                ++ga.n;
+            }
+            ++i;
+        }
+        if (ga.n == 0) {  // segment i does not fit: the ordinary update pushes what it must
+            st = blake3_hasher_update(h, d_ptrs[i], lens[i], stream);
+            if (st != B3G_OK) return st;
+            ++i;
+            continue;
+        }
+        ga.piece0[ga.n] = static_cast<uint32_t>(pieces);
+        gather_kernel<<<static_cast<unsigned>(pieces), 256, 0, s>>>(ga);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "gather_kernel launch");
+        h->acc_len += bytes;
+        h->count += bytes;
+    }
+    return B3G_OK;
+}
 
 b3g_status blake3_keyed_hash_host(const void *h_in, uint64_t len, const uint8_t key[32], uint8_t out32[32],
                                   void *d_staging, size_t staging_bytes, b3g_stream_t stream) {

@@ -121,6 +121,9 @@ def test_stream_and_xof_argument_errors(lib):
     assert lib.blake3_hasher_count(None) == 0
     lib.blake3_hasher_free(None)
     assert lib.blake3_keyed_hash_xof(FAKE, 10, None, FAKE, 32, None) == 1
+    assert lib.blake3_hasher_update_many(None, FAKE, FAKE, 1, None) == 1
+    assert lib.blake3_hasher_update_many(FAKE, None, FAKE, 1, None) == 1
+    assert lib.blake3_hasher_update_many(FAKE, FAKE, None, 1, None) == 1
     assert lib.blake3_keyed_hash_xof(FAKE, 10, KEY, None, 32, None) == 1
 
 

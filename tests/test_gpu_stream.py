@@ -229,3 +229,45 @@ def test_hasher_updates_captured_in_a_cuda_graph():
     torch.cuda.synchronize()
     assert h.count == total
     assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_hasher_update_many_matches_oracle(seed):
+    """Many device segments in one call (including empty ones, misaligned starts and a
+    few that do not fit the buffer) == the oracle digest of their concatenation."""
+    rng = np.random.default_rng(4000 + seed)
+    sizes = [int(x) for x in rng.integers(0, 3000, 300)]
+    sizes[10] = 0
+    sizes[50] = (2 << 20) + 3
+    if seed == 1:
+        sizes[100] = (70 << 20) + 5  # larger than the accumulation buffer
+    if seed == 2:
+        sizes = [int(x) for x in rng.integers(1, 700, 1500)]  # more than one launch's worth
+    total = sum(sizes)
+    host = workloads.uniform_bytes(4100 + seed, total + 64)
+    d = host.cuda()
+    segs, a = [], 0
+    for n in sizes:  # consecutive slices of one buffer: segments start at any byte
+        segs.append((a, n))
+        a += n
+    tensors = [d[x:x + n] for x, n in segs]
+    h = binding.Hasher(KEY)
+    h.update_many(tensors[:7]).update_many(tensors[7:])
+    assert h.count == total
+    assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host[:total], KEY)
+    g = binding.Hasher()
+    g.update_many(tensors)
+    assert bytes(g.finalize().cpu().numpy()) == oracle.hash(host[:total])
+
+
+def test_hasher_update_many_equals_separate_updates():
+    host = workloads.uniform_bytes(4200, 5 << 20)
+    d = host.cuda()
+    cuts = [0, 1, 1025, 4096, 70000, 70001, 1 << 20, (3 << 20) + 7, 5 << 20]
+    tensors = [d[x:y] for x, y in zip(cuts[:-1], cuts[1:])]
+    one = binding.Hasher(KEY)
+    for t in tensors:
+        one.update(t)
+    many = binding.Hasher(KEY).update_many(tensors)
+    assert bytes(one.finalize().cpu().numpy()) == bytes(many.finalize().cpu().numpy())
+    assert bytes(many.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
