@@ -404,10 +404,12 @@ def _e2e(args, binding, dev, key, out, stream, digest_api, world):
     staging = torch.empty(3328 + 2 * (256 << 20), dtype=torch.uint8, device="cuda")
     torch.cuda.synchronize()
     got = binding.blake3_keyed_hash_host(host, key, staging)  # warm-up
+    if world > 1:
+        torch.distributed.barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         got = binding.blake3_keyed_hash_host(host, key, staging)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = _max_over_ranks((time.perf_counter() - t0) / e2e_steps, world, "cuda")
     if got != digest_api:
         raise RuntimeError("end-to-end digest differs")
     # context: the host->device link alone, the same pinned buffer copied in 256 MiB
