@@ -231,7 +231,7 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD} keyed BLAKE3, uniform bytes seed 6, key seed 7",
                    "bytes": w.nbytes, "sample_bytes_per_step": sample},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -378,9 +378,10 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "vs_baseline": None, "dtype": "u32", "data": "synthetic",
         "config": {"workload": f"{w.name} keyed BLAKE3, {w.kind} bytes seed {w.data_seed}, key seed {w.key_seed}",
-                   "bytes": n, "chunks": nchunks, "leaves_per_cta": 1 << leaves_log2, "cta_roots": tiles,
+                   "input": "u8 bytes, hashed as little-endian u32 words", "bytes": n, "chunks": nchunks,
+                   "leaves_per_cta": 1 << leaves_log2, "cta_roots": tiles,
                    "l2": f"input {n / 1e9:.2f} GB > 126 MB L2; no flush needed", "parallelism": f"replicas{world}"},
         "timing": timing, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches * args.steps, "clocks": clocks,
