@@ -198,7 +198,7 @@ b3g_status hash_range_alloc(const void *d_in, uint64_t len, uint64_t chunk_offse
     const size_t need = hash_workspace(len);
     void *ws = nullptr;
     if (need) {
-        cudaError_t e = cudaMallocAsync(&ws, need, stream);
+        cudaError_t e = alloc_async(&ws, need, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
     }
     b3g_status st =
@@ -224,6 +224,34 @@ b3g_status reduce_cvs_ws(const uint8_t *d_cvs, uint64_t count, const uint32_t ke
     if (count == 0 || (count == 1 && root)) return B3G_ERR_ARG;
     if (ws_bytes < reduce_ws(count, kDefaultGroupLog2)) return B3G_ERR_WORKSPACE;
     return reduce_levels(d_cvs, count, key, mode_flags, root, kDefaultGroupLog2, d_out32, ws, stream);
+}
+
+namespace {
+// > 0: the g_fail_alloc-th next device allocation fails (then the hook is off)
+std::atomic<int64_t> g_fail_alloc{0};
+
+bool injected_failure() {
+    int64_t v = g_fail_alloc.load(std::memory_order_relaxed);
+    while (v > 0)
+        if (g_fail_alloc.compare_exchange_weak(v, v - 1, std::memory_order_relaxed)) return v == 1;
+    return false;
+}
+}  // namespace
+
+cudaError_t alloc_async(void **p, size_t bytes, cudaStream_t stream) {
+    if (injected_failure()) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMallocAsync(p, bytes, stream);
+}
+
+cudaError_t alloc_sync(void **p, size_t bytes) {
+    if (injected_failure()) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
 }
 
 b3g_status cuda_fail(cudaError_t err, const char *what) {
@@ -261,6 +289,10 @@ b3g_status blake3_set_option(b3g_option option, int64_t value) {
     switch (option) {
         case B3G_OPT_FUSED_FINAL:
             g_fused_final.store(value != 0 ? 1 : 0, std::memory_order_relaxed);
+            return B3G_OK;
+        case B3G_OPT_FAIL_ALLOC:
+            if (value < 0) return B3G_ERR_ARG;
+            g_fail_alloc.store(value, std::memory_order_relaxed);
             return B3G_OK;
     }
     return B3G_ERR_ARG;
@@ -400,7 +432,7 @@ b3g_status blake3_selftest_bounded_wait(uint32_t limit_us, int *timed_out_out) {
     if (!timed_out_out) return B3G_ERR_NULL;
     if (limit_us < 1 || limit_us > 10000000u) return B3G_ERR_ARG;
     int *d_flag = nullptr;
-    cudaError_t e = cudaMalloc(&d_flag, sizeof(int));
+    cudaError_t e = alloc_sync(reinterpret_cast<void **>(&d_flag), sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     b3g_status st = launch_wait_probe(static_cast<uint64_t>(limit_us) * 1000ull, d_flag, nullptr);
     int h = -1;

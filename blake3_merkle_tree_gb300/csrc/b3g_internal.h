@@ -90,6 +90,12 @@ b3g_status launch_wait_probe(uint64_t limit_ns, int *d_flag, cudaStream_t stream
 // Records a CUDA error for blake3_last_cuda_error() and returns B3G_ERR_CUDA.
 b3g_status cuda_fail(cudaError_t err, const char *what);
 
+// Every device allocation of the library: stream-ordered, and plain.  Both return
+// cudaErrorMemoryAllocation without allocating when the failure hook
+// (B3G_OPT_FAIL_ALLOC) selects this allocation.
+cudaError_t alloc_async(void **p, size_t bytes, cudaStream_t stream);
+cudaError_t alloc_sync(void **p, size_t bytes);
+
 // Launch with programmatic stream serialization: the grid may start while the grid
 // ahead of it in the stream is finishing.  Every kernel launched this way calls
 // grid_dependency_wait() before its first global-memory access.

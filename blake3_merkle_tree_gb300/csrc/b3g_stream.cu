@@ -578,7 +578,7 @@ b3g_status push_pieces_one_by_one(b3g_hasher *h, const uint8_t *p, const std::ve
     const size_t ws_bytes = blake3_workspace_size(biggest * kChunkBytes);
     uint8_t *ws = nullptr;
     if (ws_bytes) {
-        cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), ws_bytes, x);
+        cudaError_t e = alloc_async(reinterpret_cast<void **>(&ws), ws_bytes, x);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
     }
     const uint64_t base = h->pushed;
@@ -668,7 +668,7 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
     const size_t roots_bytes = (pieces.size() * 32 + 255) & ~size_t(255);
     const size_t tiles_bytes = (tiles * 32 + 255) & ~size_t(255);
     uint8_t *scratch = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), roots_bytes + tiles_bytes + huge_ws + 256, s);
+    cudaError_t e = alloc_async(reinterpret_cast<void **>(&scratch), roots_bytes + tiles_bytes + huge_ws + 256, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
     uint8_t *roots = scratch;
     uint8_t *tile_cvs = scratch + roots_bytes;
@@ -778,7 +778,7 @@ b3g_status append_acc(b3g_hasher *h, const uint8_t *p, uint64_t len, cudaStream_
 // 1024-byte buffer (and stops trying).
 b3g_status grow_acc(b3g_hasher *h, cudaStream_t s) {
     uint8_t *bigger = nullptr;
-    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&bigger), kAccBytes);
+    cudaError_t e = alloc_sync(reinterpret_cast<void **>(&bigger), kAccBytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
         h->may_grow = false;
@@ -823,7 +823,7 @@ b3g_status xof_range(const void *d_in, uint64_t len, const uint8_t key[32], uint
     const size_t off1 = (kStateBytes + 255) & ~size_t(255);
     const size_t off2 = off1 + ((ws_left + 255) & ~size_t(255));
     uint8_t *scratch = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), off2 + ws_right, s);
+    cudaError_t e = alloc_async(reinterpret_cast<void **>(&scratch), off2 + ws_right, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
     uint32_t *rec = reinterpret_cast<uint32_t *>(scratch + kRecordOff);
     b3g_status st;
@@ -858,7 +858,7 @@ b3g_status hasher_create(const uint8_t key[32], uint32_t mode_flags, b3g_hasher 
     hasher_clear(h);
     h->state = nullptr;
     cudaError_t e = cudaGetDevice(&h->device);
-    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void **>(&h->state), kStateBytes);
+    if (e == cudaSuccess) e = alloc_sync(reinterpret_cast<void **>(&h->state), kStateBytes);
     if (e != cudaSuccess) {
         delete h;
         return cuda_fail(e, "hasher state");
@@ -892,7 +892,7 @@ b3g_status host_range(const void *h_in, uint64_t len, const uint8_t key[32], uin
     bool own = false;
     if (!d_staging) {
         staging_bytes = kHead + 2 * (64u << 20);
-        cudaError_t e = cudaMallocAsync(&d_staging, staging_bytes, s);
+        cudaError_t e = alloc_async(&d_staging, staging_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
         own = true;
     }
@@ -1162,7 +1162,7 @@ b3g_status blake3_hasher_finalize(const b3g_hasher *hc, uint8_t *d_out, uint64_t
     uint8_t *scratch = nullptr;
     cudaError_t e;
     if (k) {
-        e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), kStateBytes, s);
+        e = alloc_async(reinterpret_cast<void **>(&scratch), kStateBytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
         if (t.depth) e = cudaMemcpyAsync(scratch, t.state, 32ull * t.depth, cudaMemcpyDeviceToDevice, s);
         if (e != cudaSuccess) st = cuda_fail(e, "cudaMemcpyAsync");

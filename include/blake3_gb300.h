@@ -85,6 +85,11 @@ typedef enum {
      * more than the launch it saves.  Applies to 16-byte aligned inputs with at least
      * one full chunk. */
     B3G_OPT_FUSED_FINAL = 1,
+    /* Test hook for failure handling (no GPU fault involved): with value n > 0, the n-th
+     * next device allocation the library makes fails as if the device were out of memory
+     * (the call returns B3G_ERR_CUDA, except a streaming hasher's optional 64 MiB buffer,
+     * which is then simply not used); afterwards the hook is off again.  0 turns it off. */
+    B3G_OPT_FAIL_ALLOC = 2,
 } b3g_option;
 
 /* Sets an option.  Errors: B3G_ERR_ARG (unknown option). */
@@ -267,7 +272,8 @@ b3g_status blake3_hasher_reset(b3g_hasher *h);
 /* Bytes absorbed so far. */
 uint64_t blake3_hasher_count(const b3g_hasher *h);
 
-/* Absorbs d_in[0..len).  Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_CUDA. */
+/* Absorbs d_in[0..len).  Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_CUDA.  After an
+ * error the hasher's contents are unspecified: reset it before using it again. */
 b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b3g_stream_t stream);
 
 /* Absorbs count device segments in order, d_ptrs[i][0..lens[i]) (host arrays of device
