@@ -70,6 +70,9 @@ def library() -> ctypes.CDLL:
             "blake3_hasher_count": (u64, [vp]),
             "blake3_hasher_update": (i32, [vp, vp, u64, vp]),
             "blake3_hasher_update_many": (i32, [vp, vp, vp, u64, vp]),
+            "blake3_hasher_export_size": (sz, [vp]),
+            "blake3_hasher_export": (i32, [vp, vp, sz, vp]),
+            "blake3_hasher_import": (i32, [vp, sz, ctypes.POINTER(vp), vp]),
             "blake3_hasher_finalize": (i32, [vp, vp, u64, vp]),
             "blake3_keyed_hash_host": (i32, [vp, u64, vp, vp, vp, sz, vp]),
             "blake3_hash": (i32, [vp, u64, vp, vp]),
@@ -330,6 +333,23 @@ class Hasher:
     @property
     def count(self) -> int:
         return int(library().blake3_hasher_count(self._h))
+
+    def export(self, stream=None) -> bytes:
+        """The hasher's whole state as bytes (checkpoint); the hasher is not changed."""
+        n = library().blake3_hasher_export_size(self._h)
+        buf = ctypes.create_string_buffer(max(1, n))
+        _check(library().blake3_hasher_export(self._h, buf, n, _stream(stream)), "blake3_hasher_export")
+        return buf.raw[:n]
+
+    @classmethod
+    def from_state(cls, state: bytes, stream=None) -> "Hasher":
+        """A hasher on the current device resumed from Hasher.export() bytes."""
+        self = cls.__new__(cls)
+        self._h = ctypes.c_void_p()
+        buf = ctypes.create_string_buffer(bytes(state), len(state))
+        _check(library().blake3_hasher_import(buf, len(state), ctypes.byref(self._h), _stream(stream)),
+               "blake3_hasher_import")
+        return self
 
     def close(self) -> None:
         if self._h:

@@ -1124,6 +1124,88 @@ b3g_status blake3_hasher_update_many(b3g_hasher *h, const void *const *d_ptrs, c
     return B3G_OK;
 }
 
+// Exported hasher state, little-endian: magic "B3GH", version, mode flags, stack depth,
+// the key (or IV) bytes, bytes absorbed, chunks pushed, bytes buffered; then the stack
+// (32 bytes per entry, bottom first) and the buffered bytes.
+constexpr uint32_t kStateMagic = 0x48473342u;  // "B3GH"
+constexpr uint32_t kStateVersion = 1;
+constexpr size_t kStateHeader = 4 * 4 + 32 + 3 * 8;
+
+size_t blake3_hasher_export_size(const b3g_hasher *h) {
+    return h ? kStateHeader + 32ull * h->depth + h->acc_len : 0;
+}
+
+b3g_status blake3_hasher_export(const b3g_hasher *h, void *h_buf, size_t buf_bytes, b3g_stream_t stream) {
+    if (!h || !h_buf) return B3G_ERR_NULL;
+    if (buf_bytes < blake3_hasher_export_size(h)) return B3G_ERR_WORKSPACE;
+    b3g_status st = check_device(h->device);
+    if (st != B3G_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    b3g_hasher t = *h;
+    st = join_all(&t, s);  // the stack is complete on `s`
+    if (st != B3G_OK) return st;
+    uint8_t *out = static_cast<uint8_t *>(h_buf);
+    const uint32_t words[4] = {kStateMagic, kStateVersion, h->mode_flags, h->depth};
+    const uint64_t counts[3] = {h->count, h->pushed, h->acc_len};
+    std::memcpy(out, words, sizeof words);
+    std::memcpy(out + 16, h->key, 32);
+    std::memcpy(out + 48, counts, sizeof counts);
+    cudaError_t e = cudaSuccess;
+    if (h->depth) e = cudaMemcpyAsync(out + kStateHeader, h->state, 32ull * h->depth, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && h->acc_len)
+        e = cudaMemcpyAsync(out + kStateHeader + 32ull * h->depth, h->acc, h->acc_len, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "hasher export");
+}
+
+b3g_status blake3_hasher_import(const void *h_buf, size_t buf_bytes, b3g_hasher **out, b3g_stream_t stream) {
+    if (!h_buf || !out) return B3G_ERR_NULL;
+    *out = nullptr;
+    if (buf_bytes < kStateHeader) return B3G_ERR_ARG;
+    const uint8_t *in = static_cast<const uint8_t *>(h_buf);
+    uint32_t words[4];
+    uint64_t counts[3];
+    uint8_t key[32];
+    std::memcpy(words, in, sizeof words);
+    std::memcpy(key, in + 16, 32);
+    std::memcpy(counts, in + 48, sizeof counts);
+    const uint32_t mode_flags = words[2], depth = words[3];
+    const uint64_t count = counts[0], pushed = counts[1], acc_len = counts[2];
+    // the record must describe a state update() can reach
+    if (words[0] != kStateMagic || words[1] != kStateVersion) return B3G_ERR_ARG;
+    if (mode_flags != kModeKeyed && mode_flags != kModeDefault) return B3G_ERR_ARG;
+    if (depth > kStackSlots - 1 || acc_len > kAccBytes || pushed > (1ull << 53)) return B3G_ERR_ARG;
+    if (count != pushed * kChunkBytes + acc_len || (pushed == 0) != (depth == 0)) return B3G_ERR_ARG;
+    if (pushed > 0 && count <= kChunkBytes) return B3G_ERR_ARG;
+    if (buf_bytes < kStateHeader + 32ull * depth + acc_len) return B3G_ERR_ARG;
+
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    b3g_hasher *h = nullptr;
+    b3g_status st = hasher_create(key, mode_flags, &h);
+    if (st != B3G_OK) return st;
+    if (acc_len > h->acc_cap) {
+        st = grow_acc(h, s);
+        if (st == B3G_OK && acc_len > h->acc_cap) st = cuda_fail(cudaErrorMemoryAllocation, "hasher import buffer");
+    }
+    cudaError_t e = cudaSuccess;
+    if (st == B3G_OK && depth)
+        e = cudaMemcpyAsync(h->state, in + kStateHeader, 32ull * depth, cudaMemcpyHostToDevice, s);
+    if (st == B3G_OK && e == cudaSuccess && acc_len)
+        e = cudaMemcpyAsync(h->acc, in + kStateHeader + 32ull * depth, acc_len, cudaMemcpyHostToDevice, s);
+    if (st == B3G_OK && e == cudaSuccess) e = cudaStreamSynchronize(s);  // the caller may free h_buf
+    if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "hasher import");
+    if (st != B3G_OK) {
+        blake3_hasher_free(h);
+        return st;
+    }
+    h->count = count;
+    h->pushed = pushed;
+    h->depth = depth;
+    h->acc_len = acc_len;
+    *out = h;
+    return B3G_OK;
+}
+
 b3g_status blake3_keyed_hash_host(const void *h_in, uint64_t len, const uint8_t key[32], uint8_t out32[32],
                                   void *d_staging, size_t staging_bytes, b3g_stream_t stream) {
     if (!key || !out32 || (!h_in && len > 0)) return B3G_ERR_NULL;

@@ -285,6 +285,22 @@ b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b
 b3g_status blake3_hasher_update_many(b3g_hasher *h, const void *const *d_ptrs, const uint64_t *lens,
                                      uint64_t count, b3g_stream_t stream);
 
+/*
+ * Checkpoint and resume.  blake3_hasher_export writes the hasher's whole state (mode,
+ * key, counts, the stack of subtree CVs and the bytes not yet pushed: at most about
+ * 64 MiB, blake3_hasher_export_size bytes) to host memory h_buf, after the work queued
+ * on `stream` (it synchronises the stream); the hasher is not changed.
+ * blake3_hasher_import creates a hasher on the current device from such a record, so
+ * that hashing can go on in another process or on another device with the same result.
+ * The record is little-endian and starts with "B3GH" and a version number.
+ * Errors: B3G_ERR_NULL; B3G_ERR_WORKSPACE (export buffer too small); B3G_ERR_ARG
+ * (import of a record that is not a state the hasher can reach: checked before any
+ * CUDA call); B3G_ERR_CUDA.
+ */
+size_t blake3_hasher_export_size(const b3g_hasher *h);
+b3g_status blake3_hasher_export(const b3g_hasher *h, void *h_buf, size_t buf_bytes, b3g_stream_t stream);
+b3g_status blake3_hasher_import(const void *h_buf, size_t buf_bytes, b3g_hasher **out, b3g_stream_t stream);
+
 /* Writes out_len bytes of output (32 for the digest) to d_out.  The hasher is not
  * changed: more input may follow.  Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_CUDA. */
 b3g_status blake3_hasher_finalize(const b3g_hasher *h, uint8_t *d_out, uint64_t out_len,

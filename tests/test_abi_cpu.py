@@ -158,3 +158,35 @@ def test_options_and_config(lib):
     assert lib.blake3_set_option(2, 0) == 0
     assert lib.blake3_set_option(1, 0) == 0
     assert lib.blake3_kernel_config().startswith(b"leaf_tma_kernel<")
+
+
+def _state_record(magic=0x48473342, version=1, mode=16, depth=1, count=3000, pushed=2, acc_len=952,
+                  extra=0):
+    import struct
+
+    head = struct.pack("<4I", magic, version, mode, depth) + bytes(32) + struct.pack("<3Q", count, pushed, acc_len)
+    return head + bytes(32 * depth + acc_len + extra)
+
+
+def test_hasher_import_rejects_bad_records_before_any_cuda_call(lib):
+    h = ctypes.c_void_p()
+
+    def imp(rec, size=None):
+        buf = ctypes.create_string_buffer(rec, len(rec))
+        return lib.blake3_hasher_import(buf, len(rec) if size is None else size, ctypes.byref(h), None)
+
+    assert lib.blake3_hasher_import(None, 100, ctypes.byref(h), None) == 1
+    assert lib.blake3_hasher_import(FAKE, 100, None, None) == 1
+    assert imp(_state_record(), size=20) == 6                     # shorter than the header
+    assert imp(_state_record(magic=0x12345678)) == 6              # not a hasher record
+    assert imp(_state_record(version=2)) == 6                     # unknown version
+    assert imp(_state_record(mode=32)) == 6                       # unknown hash mode
+    assert imp(_state_record(count=3001)) == 6                    # count != pushed * 1024 + buffered
+    assert imp(_state_record(depth=0)) == 6                       # pushed chunks but an empty stack
+    assert imp(_state_record(depth=70)) == 6                      # deeper than the stack
+    assert imp(_state_record(count=1024, pushed=1, acc_len=0)) == 6  # one chunk is never pushed
+    assert imp(_state_record(acc_len=(64 << 20) + 1, count=2048 + (64 << 20) + 1)) == 6  # buffer too large
+    rec = _state_record()
+    assert imp(rec, size=len(rec) - 1) == 6                       # truncated stack or bytes
+    assert lib.blake3_hasher_export_size(None) == 0
+    assert lib.blake3_hasher_export(None, FAKE, 100, None) == 1

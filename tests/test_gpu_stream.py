@@ -271,3 +271,29 @@ def test_hasher_update_many_equals_separate_updates():
     many = binding.Hasher(KEY).update_many(tensors)
     assert bytes(one.finalize().cpu().numpy()) == bytes(many.finalize().cpu().numpy())
     assert bytes(many.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
+
+
+@pytest.mark.parametrize("cut", [0, 700, 1024, 1025, 5000, (3 << 20) + 11, (70 << 20) + 3])
+@pytest.mark.parametrize("keyed", [True, False])
+def test_hasher_checkpoint_and_resume(cut, keyed):
+    """Export after `cut` bytes, resume in a new hasher (the old one freed), finish: the
+    digest and extendable output equal the oracle's for the whole input."""
+    total = cut + (2 << 20) + 333
+    host = workloads.uniform_bytes(7000 + cut, total)
+    d = host.cuda()
+    h = binding.Hasher(KEY if keyed else None)
+    for a in range(0, cut, 1 << 20):
+        h.update(d[a:min(cut, a + (1 << 20))])
+    state = h.export()
+    assert len(state) == binding.library().blake3_hasher_export_size(h._h)
+    before = bytes(h.finalize().cpu().numpy())
+    h.close()
+    r = binding.Hasher.from_state(state)
+    assert r.count == cut
+    assert bytes(r.finalize().cpu().numpy()) == before
+    r.update(d[cut:cut + 5]).update(d[cut + 5:])
+    ref = oracle.keyed_hash(host, KEY) if keyed else oracle.hash(host)
+    assert bytes(r.finalize().cpu().numpy()) == ref
+    xof = oracle.keyed_hash_xof(host, KEY, 96) if keyed else oracle.hash_xof(host, 96)
+    assert bytes(r.finalize(96).cpu().numpy()) == xof
+    assert r.export() != state  # the state moved on
