@@ -16,8 +16,9 @@
 //
 // GB300 design (differences from the page's Hopper design):
 //   - Persistent CTAs: the grid is sized to the resident capacity and each CTA walks
-//     tiles blockIdx.x, blockIdx.x + gridDim.x, ...; the stage ring keeps running
-//     across tiles, so the producer loads the next tile during the subtree phase.
+//     tiles blockIdx.x, blockIdx.x + gridDim.x, ...; the stage rings keep running
+//     across tiles, so the copies of the next tile are in flight while the previous
+//     tile's subtree is reduced.
 //   - No producer threads: each consumer warp feeds itself.  Its lane 0 keeps a few
 //     bulk tensor copies of the warp's own 32 chunk rows in flight in a private
 //     ring and refills a stage as soon as the warp has read it, so no warp waits

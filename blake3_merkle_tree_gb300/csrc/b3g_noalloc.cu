@@ -7,7 +7,7 @@
 // GPU at start-up), a latency-critical loop that cannot accept the device-wide
 // synchronisation cudaMalloc/cudaFree may cause, or a service whose policy forbids
 // allocation after initialisation.  blake3_keyed_hash needs a few bytes of temporary
-// device memory (one 32-byte CV per 256 chunks) and takes them from the stream-ordered
+// device memory (one 32-byte CV per CTA subtree) and takes them from the stream-ordered
 // allocator; blake3_keyed_hash_ws needs the caller to have allocated them.  This entry
 // point instead uses a fixed scratch array that is part of the library's device image:
 // it exists on every GPU that loads the library, from module load until process exit.
