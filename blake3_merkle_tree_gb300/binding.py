@@ -394,6 +394,7 @@ def blake3_hash_host(data: torch.Tensor, staging: torch.Tensor | None = None, st
 
 B3G_OPT_FUSED_FINAL = 1
 B3G_OPT_FAIL_ALLOC = 2
+B3G_OPT_STREAM_UNBATCHED = 3
 
 
 def blake3_set_option(option: int, value: int) -> None:

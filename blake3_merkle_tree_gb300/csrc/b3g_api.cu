@@ -238,6 +238,12 @@ bool injected_failure() {
 }
 }  // namespace
 
+namespace {
+std::atomic<int> g_stream_unbatched{0};
+}  // namespace
+
+bool stream_unbatched() { return g_stream_unbatched.load(std::memory_order_relaxed) != 0; }
+
 cudaError_t alloc_async(void **p, size_t bytes, cudaStream_t stream) {
     if (injected_failure()) {
         *p = nullptr;
@@ -293,6 +299,9 @@ b3g_status blake3_set_option(b3g_option option, int64_t value) {
         case B3G_OPT_FAIL_ALLOC:
             if (value < 0) return B3G_ERR_ARG;
             g_fail_alloc.store(value, std::memory_order_relaxed);
+            return B3G_OK;
+        case B3G_OPT_STREAM_UNBATCHED:
+            g_stream_unbatched.store(value != 0 ? 1 : 0, std::memory_order_relaxed);
             return B3G_OK;
     }
     return B3G_ERR_ARG;

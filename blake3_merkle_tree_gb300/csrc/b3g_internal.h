@@ -96,6 +96,9 @@ b3g_status cuda_fail(cudaError_t err, const char *what);
 cudaError_t alloc_async(void **p, size_t bytes, cudaStream_t stream);
 cudaError_t alloc_sync(void **p, size_t bytes);
 
+// B3G_OPT_STREAM_UNBATCHED: the streaming hasher's one-piece-at-a-time path is forced.
+bool stream_unbatched();
+
 // Launch with programmatic stream serialization: the grid may start while the grid
 // ahead of it in the stream is finishing.  Every kernel launched this way calls
 // grid_dependency_wait() before its first global-memory access.

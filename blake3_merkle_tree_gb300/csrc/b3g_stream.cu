@@ -650,7 +650,8 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
     }
     uint64_t big_sum = 0;
     for (size_t j : big) big_sum += pieces[j].size;
-    if (pieces.size() > static_cast<size_t>(kMaxPieces) || small.size() > static_cast<size_t>(kMaxSmallPieces) ||
+    if (stream_unbatched() || pieces.size() > static_cast<size_t>(kMaxPieces) ||
+        small.size() > static_cast<size_t>(kMaxSmallPieces) ||
         big_sum != B - A || h->depth + pieces.size() >= static_cast<size_t>(kStackSlots) ||
         (B - A) / tile > 0xffffffffull)
         return push_pieces_one_by_one(h, p, pieces, s);

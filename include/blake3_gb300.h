@@ -90,6 +90,10 @@ typedef enum {
      * (the call returns B3G_ERR_CUDA, except a streaming hasher's optional 64 MiB buffer,
      * which is then simply not used); afterwards the hook is off again.  0 turns it off. */
     B3G_OPT_FAIL_ALLOC = 2,
+    /* Test hook: 0 (default) or 1.  With 1 the streaming hasher pushes every piece of a
+     * run with its own subtree and merge launches instead of the batched launches (the
+     * path it otherwise takes only for runs beyond the batch limits). */
+    B3G_OPT_STREAM_UNBATCHED = 3,
 } b3g_option;
 
 /* Sets an option.  Errors: B3G_ERR_ARG (unknown option). */

@@ -156,6 +156,7 @@ def test_options_and_config(lib):
     assert lib.blake3_set_option(99, 1) == 6
     assert lib.blake3_set_option(2, -1) == 6  # the allocation-failure hook takes n >= 0
     assert lib.blake3_set_option(2, 0) == 0
+    assert lib.blake3_set_option(3, 1) == 0 and lib.blake3_set_option(3, 0) == 0
     assert lib.blake3_set_option(1, 0) == 0
     assert lib.blake3_kernel_config().startswith(b"leaf_tma_kernel<")
 

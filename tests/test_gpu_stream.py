@@ -297,3 +297,35 @@ def test_hasher_checkpoint_and_resume(cut, keyed):
     xof = oracle.keyed_hash_xof(host, KEY, 96) if keyed else oracle.hash_xof(host, 96)
     assert bytes(r.finalize(96).cpu().numpy()) == xof
     assert r.export() != state  # the state moved on
+
+
+@pytest.fixture
+def unbatched():
+    binding.blake3_set_option(binding.B3G_OPT_STREAM_UNBATCHED, 1)
+    yield
+    binding.blake3_set_option(binding.B3G_OPT_STREAM_UNBATCHED, 0)
+
+
+@pytest.mark.parametrize("keyed", [True, False])
+def test_hasher_unbatched_path(unbatched, keyed):
+    """The one-piece-at-a-time push (a subtree launch and a merge launch per piece, the
+    path beyond the batch limits) gives the oracle digest on ragged and large segments."""
+    total = 3 * 1024 + (70 << 20) + (5 << 20) + 777
+    host = workloads.uniform_bytes(7100 + keyed, total)
+    d = host.cuda()
+    cuts = [0, 2048, 3 * 1024 + 5, (70 << 20) + 11, (72 << 20) + 1, total]
+    h = binding.Hasher(KEY if keyed else None)
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        h.update(d[a:b])
+    ref = oracle.keyed_hash(host, KEY) if keyed else oracle.hash(host)
+    assert bytes(h.finalize().cpu().numpy()) == ref
+    rng = np.random.default_rng(7101)
+    sizes = [int(x) for x in rng.integers(1, 5000, 200)]
+    segs, a = [], 0
+    for n in sizes:
+        segs.append(d[a:a + n])
+        a += n
+    g = binding.Hasher(KEY if keyed else None)
+    g.update_many(segs)
+    g.update(d[a:])
+    assert bytes(g.finalize().cpu().numpy()) == ref
