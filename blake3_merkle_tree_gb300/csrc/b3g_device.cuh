@@ -355,6 +355,47 @@ __device__ __forceinline__ void load_block_global(const uint8_t *base, uint64_t 
     }
 }
 
+// The same block load for the plain-load kernel, which reads every block of an input
+// that is not 16-byte aligned: when the five 16-byte units covering the block lie
+// inside the buffer, five vector loads and a funnel shift per word replace the
+// seventeen word loads (one chunk per thread puts every word load of a warp on 32
+// different cache lines); otherwise load_block_global.
+__device__ __forceinline__ void load_block_units(const uint8_t *base, uint64_t len, uint64_t off, uint32_t m[16]) {
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(base) + off;
+    const uintptr_t buf_lo = reinterpret_cast<uintptr_t>(base);
+    const uintptr_t buf_hi = buf_lo + len;
+    const uintptr_t a16 = addr & ~static_cast<uintptr_t>(15);
+    if (a16 >= buf_lo && a16 + kBlockLen + 16 <= buf_hi) {
+        // every word funnel-shifted out of two neighbouring loaded words; the unit
+        // offset (r >> 2) is the same for every chunk of an input, so the switch does
+        // not diverge
+        const uint4 *p = reinterpret_cast<const uint4 *>(a16);
+        uint32_t u[20];
+#pragma unroll
+        for (int k = 0; k < 5; ++k) {
+            const uint4 w = __ldg(p + k);
+            u[4 * k + 0] = w.x;
+            u[4 * k + 1] = w.y;
+            u[4 * k + 2] = w.z;
+            u[4 * k + 3] = w.w;
+        }
+        const uint32_t r = static_cast<uint32_t>(addr & 15u);
+        const uint32_t sh = (r & 3u) * 8u;
+        switch (r >> 2) {
+#define B3G_SHIFTED_WORDS(Q)                                                            \
+    case Q:                                                                             \
+        _Pragma("unroll") for (int i = 0; i < 16; ++i) m[i] = __funnelshift_r(u[i + Q], u[i + Q + 1], sh); \
+        return;
+            B3G_SHIFTED_WORDS(0)
+            B3G_SHIFTED_WORDS(1)
+            B3G_SHIFTED_WORDS(2)
+            B3G_SHIFTED_WORDS(3)
+#undef B3G_SHIFTED_WORDS
+        }
+    }
+    load_block_global(base, len, off, m);
+}
+
 // ---------------------------------------------------------------------------------
 // CV nodes in shared memory.  Node j occupies 16-byte units 2j and 2j+1; unit k is
 // stored at k with its low three bits XORed by bits 3..5 (a 128-byte swizzle), so

@@ -520,14 +520,22 @@ __global__ void __launch_bounds__(C) leaf_direct_kernel(const LeafArgs a) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) cv[i] = key[i];
         if (valid) {
+            // the next block's loads are issued before this block's compression, so
+            // their latency hides behind it
+            uint32_t m[16];
+            load_block_units(a.in, a.len, start, m);
 #pragma unroll 1
             for (uint32_t b = 0; b < nblocks; ++b) {
-                uint32_t m[16];
-                load_block_global(a.in, a.len, start + 64ull * b, m);
                 const bool last = b + 1 == nblocks;
+                uint32_t nx[16];
+                if (!last) load_block_units(a.in, a.len, start + 64ull * (b + 1), nx);
                 const uint32_t flags = MODE | (b == 0 ? kChunkStart : 0u) | (last ? end_flags : 0u);
                 compress(cv, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32),
                          last ? last_len : 64u, flags);
+                if (!last) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) m[i] = nx[i];
+                }
             }
         }
         if constexpr (CHUNK_CVS) {

@@ -193,3 +193,19 @@ def test_fused_final_reduction_option(length):
             oracle.subtree_cv(host, KEY, 0, False)
     finally:
         binding.blake3_set_option(binding.B3G_OPT_FUSED_FINAL, 0)
+
+
+@pytest.mark.parametrize("r", list(range(1, 16)))
+def test_every_misalignment_residue(r):
+    """Inputs starting at every byte offset mod 16 take the plain-load kernel: its
+    16-byte-unit loads with shifts (inner blocks), word loads (blocks near the ends) and
+    byte loads (the ragged tail) all give the oracle's digest and chunk CVs."""
+    n = 300 * 1024 + 77
+    host = workloads.uniform_bytes(900 + r, n + 32)
+    d = host.cuda()
+    x = d[r:r + n]
+    ref = host[r:r + n]
+    assert bytes(binding.blake3_keyed_hash(x, KEY).cpu().numpy()) == oracle.keyed_hash(ref, KEY)
+    assert bytes(binding.blake3_hash(x).cpu().numpy()) == oracle.hash(ref)
+    cvs = binding.blake3_keyed_chunk_cvs(x, KEY).cpu().numpy()
+    assert (cvs == oracle.chunk_cvs(ref, KEY)).all()
