@@ -179,7 +179,7 @@ b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, con
     }
     st = launch_leaf(a, t, false, stream);
     if (st != B3G_OK) return st;
-    return reduce_levels(ws, a.n_tiles, a.key, mode_flags, root, kDefaultGroupLog2, d_out32,
+    return reduce_levels(ws, a.n_tiles, a.key, mode_flags, root, reduce_group_log2(a.n_tiles), d_out32,
                          ws + round16(a.n_tiles * 32), stream);
 }
 
@@ -188,7 +188,7 @@ size_t hash_workspace(uint64_t len) {
     const uint64_t tiles = ceil_div(n, 1ull << choose_leaves_log2(n));
     if (tiles == 1) return 0;
     // the fused path needs 16 bytes for its ticket counter instead of reduction levels
-    const size_t levels = reduce_ws(tiles, kDefaultGroupLog2);
+    const size_t levels = reduce_ws(tiles, reduce_group_log2(tiles));
     return round16(tiles * 32) + (tiles <= kMaxFusedTiles && levels < 16 ? 16 : levels);
 }
 
@@ -222,8 +222,9 @@ b3g_status hash_range_ws(const void *d_in, uint64_t len, uint64_t chunk_offset, 
 b3g_status reduce_cvs_ws(const uint8_t *d_cvs, uint64_t count, const uint32_t key[8], uint32_t mode_flags,
                          bool root, uint8_t *d_out32, uint8_t *ws, size_t ws_bytes, cudaStream_t stream) {
     if (count == 0 || (count == 1 && root)) return B3G_ERR_ARG;
-    if (ws_bytes < reduce_ws(count, kDefaultGroupLog2)) return B3G_ERR_WORKSPACE;
-    return reduce_levels(d_cvs, count, key, mode_flags, root, kDefaultGroupLog2, d_out32, ws, stream);
+    const int g = reduce_group_log2(count);
+    if (ws_bytes < reduce_ws(count, g)) return B3G_ERR_WORKSPACE;
+    return reduce_levels(d_cvs, count, key, mode_flags, root, g, d_out32, ws, stream);
 }
 
 namespace {
@@ -395,7 +396,7 @@ b3g_status blake3_keyed_tile_roots(const void *d_in, uint64_t len, uint64_t chun
 }
 
 size_t blake3_reduce_workspace_size(uint64_t count, int group_log2) {
-    if (group_log2 == -1) group_log2 = kDefaultGroupLog2;
+    if (group_log2 == -1) group_log2 = reduce_group_log2(count);
     if (group_log2 < 1 || group_log2 > kMaxGroupLog2 || count == 0) return 0;
     return reduce_ws(count, group_log2);
 }
@@ -405,7 +406,7 @@ b3g_status blake3_keyed_reduce_cvs(const uint8_t *d_cvs, uint64_t count, const u
                                    b3g_stream_t stream) {
     if (!key || !d_cvs || !d_out32) return B3G_ERR_NULL;
     if (misaligned16(d_cvs) || misaligned16(d_out32)) return B3G_ERR_ALIGN;
-    if (group_log2 == -1) group_log2 = kDefaultGroupLog2;
+    if (group_log2 == -1) group_log2 = reduce_group_log2(count);
     if (count == 0 || group_log2 < 1 || group_log2 > kMaxGroupLog2) return B3G_ERR_ARG;
     if (count == 1 && is_root) return B3G_ERR_ARG;
     const size_t need = reduce_ws(count, group_log2);

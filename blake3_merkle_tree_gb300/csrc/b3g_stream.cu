@@ -662,7 +662,7 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
     for (size_t j : big) {
         const uint64_t t = pieces[j].size / tile;
         if (t > 1024) {
-            const size_t w = blake3_reduce_workspace_size(t, 10);
+            const size_t w = blake3_reduce_workspace_size(t, -1);  // the group reduce_cvs_ws takes
             huge_ws = w > huge_ws ? w : huge_ws;
         }
     }

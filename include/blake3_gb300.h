@@ -188,7 +188,8 @@ b3g_status blake3_keyed_tile_roots(const void *d_in, uint64_t len, uint64_t chun
                                    uint8_t *d_roots, b3g_stream_t stream);
 
 /* Device workspace bytes blake3_keyed_reduce_cvs needs for `count` CVs and groups of
- * 2^group_log2 (group_log2 in 1..10, or -1 for the default 10). */
+ * 2^group_log2 (group_log2 in 1..10, or -1 for the default: 6 for at most 32,768 CVs,
+ * else 10). */
 size_t blake3_reduce_workspace_size(uint64_t count, int group_log2);
 
 /*

@@ -61,15 +61,23 @@ def test_sizes(lib):
     # the last CTA (16 bytes for its ticket counter)
     assert lib.blake3_workspace_size(1 << 20) == 32 * 32 + 16
     assert lib.blake3_workspace_size(256 * 1024) == 8 * 32 + 16
-    # 64 MiB = 65536 chunks: 128-chunk tiles already give 512 CTAs
-    assert lib.blake3_workspace_size(64 << 20) == 512 * 32
-    assert lib.blake3_workspace_size(19 << 20) == 152 * 32  # 19456 chunks / 128
-    assert lib.blake3_workspace_size(18 << 20) == 288 * 32  # 144 tiles of 128 < 152: 64-chunk tiles
-    # 4 GiB: 32768 tile CVs, then 32 group CVs
-    assert lib.blake3_workspace_size(1 << 32) == 32768 * 32 + 32 * 32
+    # up to 32,768 tile CVs the reduction takes groups of 64: 64 MiB = 65536 chunks,
+    # 128-chunk tiles already give 512 CTAs, reduced 512 -> 8 -> 1
+    assert lib.blake3_workspace_size(64 << 20) == 512 * 32 + 8 * 32
+    assert lib.blake3_workspace_size(19 << 20) == 152 * 32 + 3 * 32  # 19456 chunks / 128
+    # 144 tiles of 128 < 152: 64-chunk tiles, 288 -> 5 -> 1
+    assert lib.blake3_workspace_size(18 << 20) == 288 * 32 + 5 * 32
+    # 4 GiB: 32768 tile CVs, then 512 and 8 group CVs
+    assert lib.blake3_workspace_size(1 << 32) == 32768 * 32 + 512 * 32 + 8 * 32
+    # 12 GiB + 777: 98305 tile CVs, groups of 1024 above 32,768 CVs: 97 group CVs
+    assert lib.blake3_workspace_size(12 * (1 << 30) + 777) == 98305 * 32 + 97 * 32
     assert lib.blake3_reduce_workspace_size(1024, 10) == 0
     assert lib.blake3_reduce_workspace_size(1025, 10) == 64
     assert lib.blake3_reduce_workspace_size(5, 1) == 3 * 32 + 32 + 32
+    assert lib.blake3_reduce_workspace_size(64, -1) == 0
+    assert lib.blake3_reduce_workspace_size(2048, -1) == 32 * 32
+    assert lib.blake3_reduce_workspace_size(32768, -1) == 512 * 32 + 8 * 32
+    assert lib.blake3_reduce_workspace_size(32769, -1) == 33 * 32
 
 
 def test_argument_errors_before_any_cuda_call(lib):
