@@ -58,31 +58,45 @@ constexpr size_t kStateBytes = kRecordOff + 128;
 // root record words: cv[0..7], block[8..23], block_len[24], flags[25] (ROOT not set)
 constexpr int kRecWords = 26;
 
-// Root record of one chunk of `len` (0..1024) bytes at `p`, with counter ctr.
-__device__ void chunk_record(const uint8_t *p, uint32_t len, uint64_t ctr, const uint32_t key[8], uint32_t mode_flags,
-                             uint32_t *rec) {
+// The `len` (0..1024) bytes at `p` as 256 little-endian words, zero past len, in
+// `words`; every thread of the block takes a share of the byte loads (any alignment).
+__device__ void stage_chunk(const uint8_t *p, uint32_t len, uint32_t *words) {
+    for (uint32_t w = threadIdx.x; w < 256u; w += blockDim.x) {
+        uint32_t v = 0;
+#pragma unroll
+        for (uint32_t k = 0; k < 4; ++k) {
+            const uint32_t i = 4u * w + k;
+            if (i < len) v |= static_cast<uint32_t>(p[i]) << (8u * k);
+        }
+        words[w] = v;
+    }
+}
+
+// Root record of one chunk of `len` (0..1024) bytes, staged by stage_chunk, with
+// counter ctr: the inputs of its last compression.
+__device__ void chunk_record(const uint32_t *words, uint32_t len, uint64_t ctr, const uint32_t key[8],
+                             uint32_t mode_flags, uint32_t *rec) {
     const uint32_t nblocks = len == 0 ? 1u : (len + 63u) / 64u;
     uint32_t cv[8];
     for (int i = 0; i < 8; ++i) cv[i] = key[i];
     uint32_t m[16];
     for (uint32_t b = 0; b + 1 < nblocks; ++b) {
-        load_block_global(p, len, 64ull * b, m);
+        for (int i = 0; i < 16; ++i) m[i] = words[16 * b + i];
         compress(cv, m, static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32), 64u,
                  mode_flags | (b == 0 ? kChunkStart : 0u));
     }
     const uint32_t b = nblocks - 1;
-    load_block_global(p, len, 64ull * b, m);
     for (int i = 0; i < 8; ++i) rec[i] = cv[i];
-    for (int i = 0; i < 16; ++i) rec[8 + i] = m[i];
+    for (int i = 0; i < 16; ++i) rec[8 + i] = words[16 * b + i];
     rec[24] = len - 64u * b;
     rec[25] = mode_flags | kChunkEnd | (b == 0 ? kChunkStart : 0u);
 }
 
-// CV (no ROOT) of one chunk.
-__device__ void chunk_cv(const uint8_t *p, uint32_t len, uint64_t ctr, const uint32_t key[8], uint32_t mode_flags,
-                         uint32_t cv[8]) {
+// CV (no ROOT) of one chunk staged by stage_chunk.
+__device__ void chunk_cv(const uint32_t *words, uint32_t len, uint64_t ctr, const uint32_t key[8],
+                         uint32_t mode_flags, uint32_t cv[8]) {
     uint32_t r[kRecWords];
-    chunk_record(p, len, ctr, key, mode_flags, r);
+    chunk_record(words, len, ctr, key, mode_flags, r);
     uint32_t m[16];
     for (int i = 0; i < 8; ++i) cv[i] = r[i];
     for (int i = 0; i < 16; ++i) m[i] = r[8 + i];
@@ -133,75 +147,100 @@ struct RecordArgs {
     uint64_t piece_pos[kMaxPieces];
 };
 
-// The sequential bookkeeping of the hasher on one thread: at most 65 merges and one
-// chunk per launch.
-__global__ void record_kernel(const RecordArgs a) {
-    if (threadIdx.x != 0) return;
-    uint32_t key[8];
-    for (int i = 0; i < 8; ++i) key[i] = a.key[i];
+// The sequential bookkeeping of the hasher: at most 65 merges and one chunk per
+// launch, a chain of dependent compressions that lane 0 runs alone.  The warp first
+// stages everything the chain reads (the CV stack, the piece roots, the chunk bytes)
+// in shared memory, so that the chain pays one round of global loads instead of one
+// per step, and afterwards writes the stack back.
+__global__ void __launch_bounds__(32) record_kernel(const RecordArgs a) {
+    __shared__ uint32_t s_stack[kStackSlots * 8];
+    __shared__ uint32_t s_roots[kMaxPieces * 8];
+    __shared__ uint32_t s_chunk[256];
+    __shared__ uint32_t s_depth;
+    const uint32_t lane = threadIdx.x;
     uint32_t *stack = reinterpret_cast<uint32_t *>(a.state);
     uint32_t *rec = reinterpret_cast<uint32_t *>(a.state + kRecordOff);
-    switch (a.mode) {
-        case kRecChunk:
-            chunk_record(a.in, a.len, a.pushed, key, a.mode_flags, rec);
-            return;
-        case kRecMerge:
-            merge_down(stack, a.depth, a.target, key, a.mode_flags);
-            return;
-        case kRecPush: {
-            const uint32_t d = merge_down(stack, a.depth, a.target, key, a.mode_flags);
-            uint32_t cv[8];
-            chunk_cv(a.in, 1024u, a.pushed, key, a.mode_flags, cv);
-            for (int i = 0; i < 8; ++i) stack[8 * d + i] = cv[i];
-            return;
-        }
-        case kRecPushMany: {
-            uint32_t d = a.depth;
-            for (uint32_t j = 0; j < a.npieces; ++j) {
-                d = merge_down(stack, d, static_cast<uint32_t>(__popcll(a.piece_pos[j])), key, a.mode_flags);
-                const uint32_t *rw = reinterpret_cast<const uint32_t *>(a.roots + 32ull * j);
-                for (int i = 0; i < 8; ++i) stack[8 * d + i] = rw[i];
-                ++d;
-            }
-            return;
-        }
-        case kRecParent:
-            for (int i = 0; i < 8; ++i) rec[i] = key[i];
-            rec[24] = kBlockLen;
-            rec[25] = a.mode_flags | kParent;
-            return;
-        case kRecFinalize: {
-            uint32_t st[kStackSlots * 8];  // a private copy: the hasher state is not changed
-            for (uint32_t i = 0; i < 8 * a.depth; ++i) st[i] = stack[i];
-            uint32_t d = a.depth;
-            uint64_t n = a.pushed;
-            if (a.len > 0) {  // the unfinished chunk becomes the last leaf
-                d = merge_down(st, d, static_cast<uint32_t>(__popcll(n)), key, a.mode_flags);
-                chunk_cv(a.in, a.len, n, key, a.mode_flags, st + 8 * d);
-                ++d;
-                ++n;
-            }
-            const uint32_t pc = static_cast<uint32_t>(__popcll(n));
-            d = merge_down(st, d, pc < 2 ? 2u : pc, key, a.mode_flags);
-            uint32_t cv[8];
-            for (int i = 0; i < 8; ++i) cv[i] = st[8 * (d - 1) + i];
-            for (uint32_t e = d - 1; e > 1; --e) {
-                uint32_t l[8];
-                for (int i = 0; i < 8; ++i) l[i] = st[8 * (e - 1) + i];
-                parent(key, a.mode_flags, l, cv, false, cv);
-            }
-            for (int i = 0; i < 8; ++i) {
-                rec[i] = key[i];
-                rec[8 + i] = st[i];
-                rec[16 + i] = cv[i];
-            }
-            rec[24] = kBlockLen;
-            rec[25] = a.mode_flags | kParent;
-            return;
-        }
-        default:
-            return;
+    const bool reads_stack = a.mode == kRecMerge || a.mode == kRecPush || a.mode == kRecPushMany ||
+                             a.mode == kRecFinalize;
+    if (reads_stack)
+        for (uint32_t i = lane; i < 8u * a.depth; i += 32u) s_stack[i] = stack[i];
+    if (a.mode == kRecPushMany) {
+        const uint32_t *rw = reinterpret_cast<const uint32_t *>(a.roots);
+        for (uint32_t i = lane; i < 8u * a.npieces; i += 32u) s_roots[i] = rw[i];
     }
+    if (a.mode == kRecChunk || (a.mode == kRecFinalize && a.len > 0)) stage_chunk(a.in, a.len, s_chunk);
+    if (a.mode == kRecPush) stage_chunk(a.in, 1024u, s_chunk);
+    __syncwarp();
+
+    if (lane == 0) {
+        uint32_t key[8];
+        for (int i = 0; i < 8; ++i) key[i] = a.key[i];
+        uint32_t keep = 0;  // stack entries to write back
+        switch (a.mode) {
+            case kRecChunk:
+                chunk_record(s_chunk, a.len, a.pushed, key, a.mode_flags, rec);
+                break;
+            case kRecMerge:
+                keep = merge_down(s_stack, a.depth, a.target, key, a.mode_flags);
+                break;
+            case kRecPush: {
+                const uint32_t d = merge_down(s_stack, a.depth, a.target, key, a.mode_flags);
+                chunk_cv(s_chunk, 1024u, a.pushed, key, a.mode_flags, s_stack + 8 * d);
+                keep = d + 1;
+                break;
+            }
+            case kRecPushMany: {
+                uint32_t d = a.depth;
+                for (uint32_t j = 0; j < a.npieces; ++j) {
+                    d = merge_down(s_stack, d, static_cast<uint32_t>(__popcll(a.piece_pos[j])), key, a.mode_flags);
+                    for (int i = 0; i < 8; ++i) s_stack[8 * d + i] = s_roots[8 * j + i];
+                    ++d;
+                }
+                keep = d;
+                break;
+            }
+            case kRecParent:
+                for (int i = 0; i < 8; ++i) rec[i] = key[i];
+                rec[24] = kBlockLen;
+                rec[25] = a.mode_flags | kParent;
+                break;
+            case kRecFinalize: {
+                // the staged stack is a private copy: the hasher state is not changed
+                uint32_t *st = s_stack;
+                uint32_t d = a.depth;
+                uint64_t n = a.pushed;
+                if (a.len > 0) {  // the unfinished chunk becomes the last leaf
+                    d = merge_down(st, d, static_cast<uint32_t>(__popcll(n)), key, a.mode_flags);
+                    chunk_cv(s_chunk, a.len, n, key, a.mode_flags, st + 8 * d);
+                    ++d;
+                    ++n;
+                }
+                const uint32_t pc = static_cast<uint32_t>(__popcll(n));
+                d = merge_down(st, d, pc < 2 ? 2u : pc, key, a.mode_flags);
+                uint32_t cv[8];
+                for (int i = 0; i < 8; ++i) cv[i] = st[8 * (d - 1) + i];
+                for (uint32_t e = d - 1; e > 1; --e) {
+                    uint32_t l[8];
+                    for (int i = 0; i < 8; ++i) l[i] = st[8 * (e - 1) + i];
+                    parent(key, a.mode_flags, l, cv, false, cv);
+                }
+                for (int i = 0; i < 8; ++i) {
+                    rec[i] = key[i];
+                    rec[8 + i] = st[i];
+                    rec[16 + i] = cv[i];
+                }
+                rec[24] = kBlockLen;
+                rec[25] = a.mode_flags | kParent;
+                break;
+            }
+            default:
+                break;
+        }
+        s_depth = keep;
+    }
+    __syncwarp();
+    const uint32_t keep = s_depth;
+    for (uint32_t i = lane; i < 8u * keep; i += 32u) stack[i] = s_stack[i];
 }
 
 // Small pieces (at most 64 full chunks each, counters from `counter`), one CTA per
