@@ -339,20 +339,27 @@ __global__ void __launch_bounds__(512) ranges_reduce_kernel(const RangesArgs a) 
 // dst + off[j]; the copy is cut into pieces of kGatherPiece bytes, piece0[j] being
 // segment j's first piece, and CTA i copies piece i.  A piece whose source and
 // destination share their alignment modulo 16 moves 16-byte words between a byte head
-// and a byte tail; any other piece moves bytes.
-constexpr int kGatherMax = 128;
+// and a byte tail; any other piece moves bytes.  The segment table travels in the
+// kernel parameters: K = 128 entries (3.6 KB) for short calls, K = 1024 (28 KB, under
+// the 32,764-byte parameter limit) when more segments are waiting, so that a call with
+// many small segments needs an eighth of the launches.
+constexpr int kGatherSmall = 128;
+constexpr int kGatherBig = 1024;
 constexpr uint32_t kGatherPiece = 32 * 1024;
 
+template <int K>
 struct GatherArgs {
     uint8_t *dst;
     uint32_t n;
-    const uint8_t *src[kGatherMax];
-    uint64_t off[kGatherMax];
-    uint64_t len[kGatherMax];
-    uint32_t piece0[kGatherMax + 1];
+    const uint8_t *src[K];
+    uint64_t off[K];
+    uint64_t len[K];
+    uint32_t piece0[K + 1];
 };
+static_assert(sizeof(GatherArgs<kGatherBig>) <= 32764, "kernel parameter limit");
 
-__global__ void __launch_bounds__(256) gather_kernel(const GatherArgs a) {
+template <int K>
+__global__ void __launch_bounds__(256) gather_kernel(const GatherArgs<K> a) {
     const uint32_t piece = blockIdx.x;
     uint32_t lo = 0, hi = a.n;  // the segment j with piece0[j] <= piece < piece0[j + 1]
     while (hi - lo > 1) {
@@ -1000,6 +1007,43 @@ b3g_status host_range(const void *h_in, uint64_t len, const uint8_t key[32], uin
 
 }  // namespace
 
+namespace {
+
+// One gather launch: segments i, i+1, ... (up to K, skipping empty ones) while they fit
+// in the accumulation buffer; advances i past them.  `launched` is false when segment
+// i itself does not fit (nothing launched, i unchanged).
+template <int K>
+b3g_status gather_run(b3g_hasher *h, const void *const *d_ptrs, const uint64_t *lens, uint64_t count, uint64_t &i,
+                      bool &launched, cudaStream_t s) {
+    GatherArgs<K> ga;
+    ga.dst = h->acc + h->acc_len;
+    ga.n = 0;
+    uint64_t bytes = 0, pieces = 0;
+    while (i < count && ga.n < static_cast<uint32_t>(K) && h->acc_len + bytes + lens[i] <= h->acc_cap) {
+        if (lens[i] > 0) {
+            ga.src[ga.n] = static_cast<const uint8_t *>(d_ptrs[i]);
+            ga.off[ga.n] = bytes;
+            ga.len[ga.n] = lens[i];
+            ga.piece0[ga.n] = static_cast<uint32_t>(pieces);
+            pieces += (lens[i] + kGatherPiece - 1) / kGatherPiece;
+            bytes += lens[i];
+            ++ga.n;
+        }
+        ++i;
+    }
+    launched = ga.n > 0;
+    if (!launched) return B3G_OK;
+    ga.piece0[ga.n] = static_cast<uint32_t>(pieces);
+    gather_kernel<K><<<static_cast<unsigned>(pieces), 256, 0, s>>>(ga);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "gather_kernel launch");
+    h->acc_len += bytes;
+    h->count += bytes;
+    return B3G_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 b3g_status blake3_keyed_hash_xof(const void *d_in, uint64_t len, const uint8_t key[32], uint8_t *d_out,
@@ -1132,34 +1176,16 @@ b3g_status blake3_hasher_update_many(b3g_hasher *h, const void *const *d_ptrs, c
             if (st != B3G_OK) return st;
         }
         // the run of segments that fit in the accumulation buffer: one gather launch
-        GatherArgs ga;
-        ga.dst = h->acc + h->acc_len;
-        ga.n = 0;
-        uint64_t bytes = 0, pieces = 0;
-        while (i < count && ga.n < static_cast<uint32_t>(kGatherMax) && h->acc_len + bytes + lens[i] <= h->acc_cap) {
-            if (lens[i] > 0) {
-                ga.src[ga.n] = static_cast<const uint8_t *>(d_ptrs[i]);
-                ga.off[ga.n] = bytes;
-                ga.len[ga.n] = lens[i];
-                ga.piece0[ga.n] = static_cast<uint32_t>(pieces);
-                pieces += (lens[i] + kGatherPiece - 1) / kGatherPiece;
-                bytes += lens[i];
-                ++ga.n;
-            }
-            ++i;
-        }
-        if (ga.n == 0) {  // segment i does not fit: the ordinary update pushes what it must
+        bool launched = false;
+        st = count - i > static_cast<uint64_t>(kGatherSmall)
+                 ? gather_run<kGatherBig>(h, d_ptrs, lens, count, i, launched, s)
+                 : gather_run<kGatherSmall>(h, d_ptrs, lens, count, i, launched, s);
+        if (st != B3G_OK) return st;
+        if (!launched) {  // segment i does not fit: the ordinary update pushes what it must
             st = blake3_hasher_update(h, d_ptrs[i], lens[i], stream);
             if (st != B3G_OK) return st;
             ++i;
-            continue;
         }
-        ga.piece0[ga.n] = static_cast<uint32_t>(pieces);
-        gather_kernel<<<static_cast<unsigned>(pieces), 256, 0, s>>>(ga);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail(e, "gather_kernel launch");
-        h->acc_len += bytes;
-        h->count += bytes;
     }
     return B3G_OK;
 }

@@ -284,7 +284,8 @@ b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b
 /* Absorbs count device segments in order, d_ptrs[i][0..lens[i]) (host arrays of device
  * pointers and lengths), with the result of count blake3_hasher_update calls.  Runs of
  * segments that fit in the accumulation buffer are copied by one gather launch per up
- * to 128 segments, so many small segments cost one launch instead of one copy each.
+ * to 1024 segments (128 when fewer are left), so many small segments cost one launch
+ * instead of one copy each.
  * Errors: B3G_ERR_NULL (h NULL; d_ptrs or lens NULL with count > 0; a NULL pointer with
  * a nonzero length), B3G_ERR_ARG, B3G_ERR_CUDA. */
 b3g_status blake3_hasher_update_many(b3g_hasher *h, const void *const *d_ptrs, const uint64_t *lens,

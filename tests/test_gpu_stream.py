@@ -231,7 +231,7 @@ def test_hasher_updates_captured_in_a_cuda_graph():
     assert bytes(h.finalize().cpu().numpy()) == oracle.keyed_hash(host, KEY)
 
 
-@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
 def test_hasher_update_many_matches_oracle(seed):
     """Many device segments in one call (including empty ones, misaligned starts and a
     few that do not fit the buffer) == the oracle digest of their concatenation."""
@@ -243,6 +243,8 @@ def test_hasher_update_many_matches_oracle(seed):
         sizes[100] = (70 << 20) + 5  # larger than the accumulation buffer
     if seed == 2:
         sizes = [int(x) for x in rng.integers(1, 700, 1500)]  # more than one launch's worth
+    if seed == 3:  # two full 1024-segment launches, then a 128-segment one
+        sizes = [int(x) for x in rng.integers(1, 400, 2100)]
     total = sum(sizes)
     host = workloads.uniform_bytes(4100 + seed, total + 64)
     d = host.cuda()
