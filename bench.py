@@ -143,9 +143,27 @@ def _max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
-def _job_gbs(bytes_per_rank: int, steps: int, total_ms: float, world: int) -> float:
-    """Whole-job GB/s: every rank hashes its own copy of the workload (weak scaling)."""
-    return world * bytes_per_rank * steps / (total_ms / 1e3) / 1e9
+def _job_gbs(job_bytes: int, steps: int, total_ms: float) -> float:
+    """Whole-job GB/s: the bytes all ranks hash per step, over the slowest rank's time."""
+    return job_bytes * steps / (total_ms / 1e3) / 1e9
+
+
+def _reduce_launches(count: int) -> int:
+    """Launches of the root reduction of `count` CVs (groups of 64 up to 32,768 CVs, else 1024)."""
+    group = 64 if count <= 32768 else 1024
+    launches = 0
+    while count > 1:
+        count = -(-count // group)
+        launches += 1
+    return launches
+
+
+def _leaf_compressions(nbytes: int, tiles: int) -> int:
+    """Compressions of the leaf kernel over `nbytes` in `tiles` 128-chunk subtrees: 16 per
+    full chunk, one per block of the partial chunk, and the parents inside the subtrees."""
+    nchunks = max(1, -(-nbytes // 1024))
+    tail = nbytes % 1024
+    return (nbytes // 1024) * 16 + ((tail + 63) // 64 if tail else 0) + (nchunks - tiles)
 
 
 def _dist():
@@ -248,9 +266,7 @@ def run_ours(args):
 
     world, rank, local = _dist()
     if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl")
+        return run_sharded(args, world, rank, local)
     torch.cuda.set_device(local)
     build.build()
     lib = binding.library()
@@ -282,12 +298,7 @@ def run_ours(args):
             if st:
                 raise binding.B3GError(st, "blake3_keyed_reduce_cvs")
 
-    # reduction launches per step: ceil-divide by 1024 until one CV is left
-    launches = 1
-    c = tiles
-    while c > 1:
-        c = -(-c // 1024)
-        launches += 1
+    launches = 1 + _reduce_launches(tiles)  # per step: the leaf launch and the reduction levels
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -300,8 +311,6 @@ def run_ours(args):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     end = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
     torch.cuda.synchronize()
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     gpu_id = str(getattr(props, "uuid", "") or "")
@@ -310,23 +319,20 @@ def run_ours(args):
             step(starts[i], mids[i])
         end.record(stream)
         torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
     total_ms = starts[0].elapsed_time(end)
     leaf_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
     step_ms = [starts[i].elapsed_time(starts[i + 1] if i + 1 < args.steps else end) for i in range(args.steps)]
     timing = {"step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
               "leaf_ms_median": statistics.median(leaf_ms),
               "reduction_and_gaps_ms_median": statistics.median(s - l for s, l in zip(step_ms, leaf_ms))}
-    total_ms = _max_over_ranks(total_ms, world, "cuda")
     ms_per_step = total_ms / args.steps
-    value = _job_gbs(n, args.steps, total_ms, world)
+    value = _job_gbs(n, args.steps, total_ms)
 
     # roofline of the leaf kernel (integer issue bound)
     nchunks = max(1, -(-n // 1024))
     nfull = n // 1024
     tail = n % 1024
-    leaf_compressions = nfull * 16 + ((tail + 63) // 64 if tail else 0) + (nchunks - tiles)
+    leaf_compressions = _leaf_compressions(n, tiles)
     ops = leaf_compressions * OPS_PER_COMPRESSION
     page_ops = leaf_compressions * PAGE_OPS_PER_COMPRESSION
     leaf_s = statistics.mean(leaf_ms) / 1e3
@@ -362,10 +368,10 @@ def run_ours(args):
     e2e = None
     host = None
     if not args.no_e2e:
-        e2e, host = _e2e(args, binding, dev, key, out, stream, digest_api, world)
+        e2e, host = _e2e(args, binding, dev, key, digest_api)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         if host is None:
             host = dev.cpu()
         sample, dt = _oracle_sample(host, key, args.cpu_seconds)
@@ -383,13 +389,125 @@ def run_ours(args):
         "config": {"workload": f"{w.name} keyed BLAKE3, {w.kind} bytes seed {w.data_seed}, key seed {w.key_seed}",
                    "input": "u8 bytes, hashed as little-endian u32 words", "bytes": n, "chunks": nchunks,
                    "leaves_per_cta": 1 << leaves_log2, "cta_roots": tiles,
-                   "l2": f"input {n / 1e9:.2f} GB > 126 MB L2; no flush needed", "parallelism": f"replicas{world}"},
+                   "l2": f"input {n / 1e9:.2f} GB > 126 MB L2; no flush needed", "parallelism": "one GPU"},
         "timing": timing, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches * args.steps, "clocks": clocks,
         "digest": digest_api.hex(),
     }
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_sharded(args, world, rank, local):
+    """N > 1: one buffer of N times the workload's length (bytes [0, N * len) of the same
+    seeded stream), sharded over the ranks in 128-chunk tiles, so every GPU holds the
+    workload's length give or take one tile (weak scaling).  A step is the leaf launch on
+    the rank's slice, an all-gather of the tile roots over NCCL and the fold to the ROOT
+    digest on every rank (blake3_merkle_tree_gb300.sharded)."""
+    import torch.distributed as dist
+    from blake3_merkle_tree_gb300 import binding, build, sharded
+
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    lib = binding.library()
+    w = workloads.WORKLOADS[args.workload]
+    if w.kind != "uniform":
+        raise SystemExit(f"{w.name}: the sharded run needs a uniform workload")
+    key = w.key()
+    total = world * w.nbytes
+    sd = sharded.ShardedDigest(total, key)
+    n_loc = sd.end - sd.start
+    n_tiles = sd.t1 - sd.t0
+    dev = w.data_range(sd.start, n_loc, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(3, args.warmup)):
+        sd(dev)
+    torch.cuda.synchronize()
+    digest = bytes(sd.out.cpu().numpy())
+    mine = torch.tensor(list(digest), dtype=torch.uint8, device="cuda")
+    every = [torch.empty_like(mine) for _ in range(world)]
+    dist.all_gather(every, mine)
+    if any(bytes(x.cpu().numpy()) != digest for x in every):
+        raise RuntimeError("the ranks disagree on the sharded digest")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    end = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    gpu_id = str(getattr(props, "uuid", "") or "")
+    with ClockSampler(gpu_id) as clk:
+        for i in range(args.steps):
+            starts[i].record(stream)
+            sd(dev, after_leaf=lambda e=mids[i]: e.record(stream))
+        end.record(stream)
+        torch.cuda.synchronize()
+    dist.barrier()
+    total_ms = _max_over_ranks(starts[0].elapsed_time(end), world, "cuda")
+    leaf_ms = [starts[i].elapsed_time(mids[i]) for i in range(args.steps)]
+    step_ms = [starts[i].elapsed_time(starts[i + 1] if i + 1 < args.steps else end) for i in range(args.steps)]
+    timing = {"step_ms_median": statistics.median(step_ms), "step_ms_min": min(step_ms),
+              "leaf_ms_median": statistics.median(leaf_ms),
+              "gather_and_fold_ms_median": statistics.median(x - y for x, y in zip(step_ms, leaf_ms)),
+              "note": "this rank's (rank 0's) events; the value uses the slowest rank's total"}
+    value = _job_gbs(total, args.steps, total_ms)
+
+    # roofline of this rank's leaf launch (integer issue bound)
+    peaks, peak_kind = _peaks()
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    peak_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    int_peak = sms * INT32_LANES_PER_SM * peak_mhz * 1e6
+    leaf_s = statistics.mean(leaf_ms) / 1e3
+    ops = _leaf_compressions(n_loc, n_tiles) * OPS_PER_COMPRESSION
+    nchunks = max(1, -(-n_loc // 1024))
+    traffic, traffic_src, _ = _traffic_per_launch(lib, nchunks)
+    roofline = {"bound": "alu", "achieved": ops / leaf_s / 1e9, "peak": int_peak / 1e9, "unit": "Gop/s",
+                "frac": ops / leaf_s / int_peak, "traffic": traffic, "traffic_source": traffic_src,
+                "ops_per_launch": ops, "leaf_ms": statistics.mean(leaf_ms), "algorithmic_bytes": n_loc,
+                "peak_basis": f"{sms} SMs x {INT32_LANES_PER_SM} int32 lanes x {peak_mhz:.0f} MHz (derived)",
+                "peak_kind": peak_kind, "kernel_config": lib.blake3_kernel_config().decode()}
+
+    # end to end: each rank's slice from pinned host memory, copies overlapped with the
+    # leaf launches, then the gather, the fold and the 32-byte digest back to the host
+    e2e = None
+    if not args.no_e2e:
+        host = torch.empty(n_loc, dtype=torch.uint8, pin_memory=True)
+        host.copy_(dev)
+        sd.from_host(host)
+        torch.cuda.synchronize()
+        dist.barrier()
+        step_s = []
+        for _ in range(max(1, min(args.e2e_steps, args.steps))):
+            t0 = time.perf_counter()
+            got = bytes(sd.from_host(host).cpu().numpy())
+            step_s.append(time.perf_counter() - t0)
+            if got != digest:
+                raise RuntimeError("end-to-end sharded digest differs")
+        e2e_s = _max_over_ranks(statistics.median(step_s), world, "cuda")
+        e2e = {"value": total / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": total,
+               "d2h_bytes_per_step": 32 * world, "ms_per_step": e2e_s * 1e3, "steps": len(step_s),
+               "ms_each_step": [round(x * 1e3, 2) for x in step_s], "statistic": "median step, slowest rank",
+               "call": "ShardedDigest.from_host (pinned host slice per rank, 2 x 256 MiB device slots)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": {"workload": f"{world} x {w.name} keyed BLAKE3 as one buffer, {w.kind} bytes seed {w.data_seed}, "
+                               f"key seed {w.key_seed}",
+                   "input": "u8 bytes, hashed as little-endian u32 words", "bytes": total,
+                   "bytes_this_rank": n_loc, "tiles": sd.tiles, "tiles_this_rank": n_tiles,
+                   "l2": f"input {n_loc / 1e9:.2f} GB per GPU > 126 MB L2; no flush needed",
+                   "parallelism": f"sharded{world}",
+                   "exchange": "all-gather of the 32-byte tile roots over NCCL, fold on every rank"},
+        "timing": timing, "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
+        "gpu_launches": (int(n_tiles > 0) + _reduce_launches(sd.tiles)) * args.steps,
+        "clocks": clk.summary(), "digest": digest.hex(),
+    }
+    dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -411,7 +529,7 @@ def _h2d_link_gbs(dev, host, warm=True):
     return n / (time.perf_counter() - c0) / 1e9
 
 
-def _e2e(args, binding, dev, key, out, stream, digest_api, world):
+def _e2e(args, binding, dev, key, digest_api):
     """The digest of the workload from pinned host memory through blake3_keyed_hash_host:
     every step copies the whole input host->device (overlapped with hashing inside the
     call) and returns the 32-byte digest to the host.  Each step is timed on its own and
@@ -425,8 +543,6 @@ def _e2e(args, binding, dev, key, out, stream, digest_api, world):
     torch.cuda.synchronize()
     link_before = _h2d_link_gbs(dev, host)
     got = binding.blake3_keyed_hash_host(host, key, staging)  # warm-up
-    if world > 1:
-        torch.distributed.barrier()
     step_s, link_each = [], []
     for _ in range(e2e_steps):
         t0 = time.perf_counter()
@@ -435,9 +551,9 @@ def _e2e(args, binding, dev, key, out, stream, digest_api, world):
         if got != digest_api:
             raise RuntimeError("end-to-end digest differs")
         link_each.append(_h2d_link_gbs(dev, host, warm=False))  # the link alone, right after
-    e2e_s = _max_over_ranks(statistics.median(step_s), world, "cuda")
+    e2e_s = statistics.median(step_s)
     link_after = _h2d_link_gbs(dev, host)
-    e2e = {"value": world * n / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": n,
+    e2e = {"value": n / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": n,
            "d2h_bytes_per_step": 32, "ms_per_step": e2e_s * 1e3, "steps": e2e_steps,
            "ms_each_step": [round(x * 1e3, 2) for x in step_s], "statistic": "median step",
            "h2d_copy_GBps_after_each_step": [round(x, 1) for x in link_each],

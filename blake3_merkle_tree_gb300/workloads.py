@@ -75,12 +75,15 @@ def _splitmix_words_torch(seed: int, start: int, count: int, device) -> torch.Te
 
 
 def uniform_bytes(seed: int, nbytes: int, device="cpu", out: torch.Tensor | None = None,
-                  slice_bytes: int = 1 << 28) -> torch.Tensor:
-    """``nbytes`` uniform bytes of stream ``seed`` as a uint8 tensor on ``device``.
+                  slice_bytes: int = 1 << 28, start: int = 0) -> torch.Tensor:
+    """``nbytes`` uniform bytes of stream ``seed``, from byte ``start`` on (a multiple of
+    8), as a uint8 tensor on ``device``.
 
     Made slice by slice (``slice_bytes`` at a time) to bound the temporaries.
     If ``out`` is given it must be a contiguous uint8 tensor of ``nbytes`` elements.
     """
+    if start % 8:
+        raise ValueError("start must be a multiple of 8")
     if out is None:
         out = torch.empty(nbytes, dtype=torch.uint8, device=device)
     assert out.numel() == nbytes and out.dtype == torch.uint8 and out.is_contiguous()
@@ -89,7 +92,7 @@ def uniform_bytes(seed: int, nbytes: int, device="cpu", out: torch.Tensor | None
     while pos < nbytes:
         take = min(slice_bytes, nbytes - pos)
         nwords = (take + 7) // 8
-        words = _splitmix_words_torch(seed, pos // 8, nwords, out.device)
+        words = _splitmix_words_torch(seed, (start + pos) // 8, nwords, out.device)
         # int64 -> little-endian bytes (both CPU and GB300 are little-endian)
         out[pos:pos + take].copy_(words.view(torch.uint8)[:take])
         pos += take
@@ -137,6 +140,13 @@ class Workload:
                 return out
             return b.to(device)
         return uniform_bytes(self.data_seed, self.nbytes, device=device, out=out)
+
+    def data_range(self, start: int, nbytes: int, device="cpu") -> torch.Tensor:
+        """Bytes [start, start + nbytes) of this workload's stream, which continues past
+        ``self.nbytes`` (a larger buffer of the same kind); uniform workloads only."""
+        if self.kind != "uniform":
+            raise ValueError("byte ranges are defined for uniform workloads only")
+        return uniform_bytes(self.data_seed, nbytes, device=device, start=start)
 
 
 WORKLOADS = {

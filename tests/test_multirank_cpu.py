@@ -1,8 +1,9 @@
 """The N > 1 host logic of bench.py on the CPU: two gloo ranks, and torchrun with two ranks.
 
-The path runs as independent replicas (one full digest per GPU, no data-path collective);
-what several ranks share is the timing: a barrier around the timed region, the maximum
-time over ranks, and the whole-job throughput over all ranks' bytes.
+With N ranks the digest is sharded (blake3_merkle_tree_gb300.sharded, tested with gloo
+ranks in test_sharded_cpu.py); what the ranks share in the bench is the timing: a barrier
+around the timed region, the maximum time over ranks, and the whole-job throughput over
+all ranks' bytes.
 """
 
 import json
@@ -34,7 +35,7 @@ def _rank_main(rank, world, port, local_ms, q):
     try:
         dist.barrier()
         slowest = bench._max_over_ranks(local_ms[rank], world, "cpu")
-        value = bench._job_gbs(1 << 30, 4, slowest, world)
+        value = bench._job_gbs(world * (1 << 30), 4, slowest)
         dist.barrier()
         q.put((rank, slowest, value))
     finally:
@@ -67,7 +68,20 @@ def test_single_rank_needs_no_process_group():
     import bench
 
     assert bench._max_over_ranks(3.25, 1, "cpu") == 3.25
-    assert bench._job_gbs(10 ** 9, 2, 1000.0, 1) == pytest.approx(2.0)
+    assert bench._job_gbs(10 ** 9, 2, 1000.0) == pytest.approx(2.0)
+
+
+def test_launch_and_work_counts():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    # reduction launches: groups of 64 CVs up to 32,768, else 1024
+    assert [bench._reduce_launches(c) for c in (1, 32, 64, 65, 2048, 32768, 32769, 98305)] == \
+        [0, 1, 1, 2, 2, 3, 2, 2]
+    # 12 GiB + 777: 16 per full chunk, 13 blocks of the 777-byte chunk, parents inside tiles
+    n = 12 * (1 << 30) + 777
+    assert bench._leaf_compressions(n, 98305) == 12582912 * 16 + 13 + (12582913 - 98305)
+    assert bench._leaf_compressions(1 << 20, 8) == 1024 * 16 + 1024 - 8
 
 
 def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
