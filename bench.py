@@ -166,6 +166,27 @@ def _leaf_compressions(nbytes: int, tiles: int) -> int:
     return (nbytes // 1024) * 16 + ((tail + 63) // 64 if tail else 0) + (nchunks - tiles)
 
 
+def _cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.machine()
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -253,7 +274,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD} keyed BLAKE3, uniform bytes seed 6, key seed 7",
                    "bytes": w.nbytes, "sample_bytes_per_step": sample},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu_model": _cpu_model(),
                          "sample": f"first {sample} bytes of the workload, hashed as a whole input, per step"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -375,7 +396,7 @@ def run_ours(args):
         if host is None:
             host = dev.cpu()
         sample, dt = _oracle_sample(host, key, args.cpu_seconds)
-        cpu = {"value": sample / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": sample / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu_model": _cpu_model(),
                "sample": f"first {sample} bytes of the workload hashed as one input by the single-threaded "
                          f"C oracle ({dt:.1f} s)"}
         cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
