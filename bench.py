@@ -677,6 +677,31 @@ def run_mode(args):
                 "value": d.numel() / ms / 1e6, "unit": "GB/s", "ms_per_digest": ms,
                 "keyed_GBps": d.numel() / ms_keyed / 1e6,
                 "config": {"workload": w.name, "call": "blake3_hash_ws / blake3_keyed_hash_ws"}}
+    elif args.mode == "ceiling":
+        # the compression alone (messages in registers, no loads, no tree): the ceiling the
+        # leaf kernel runs against, at its own 20 consumer warps per SM and at 32
+        props = torch.cuda.get_device_properties(0)
+        sms = props.multi_processor_count
+        sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+        iters = 256
+        rates = {}
+        for warps in (20, 32):
+            blocks = sms * warps // 4
+            ms = _timed(lambda b=blocks: binding.blake3_selftest_compress_rate(b, iters, sink), args.steps,
+                        args.warmup)
+            rates[warps] = blocks * 128 * iters / (ms / 1e3)
+        peaks, _ = _peaks()
+        mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        # XORs and rotates have only the ALU pipe (16 lanes per scheduler): 456 per compression
+        alu_bound = sms * mhz * 1e6 * 64 / 456
+        line = {"mode": "ceiling", "metric": "compressions/s, messages in registers (keyed BLAKE3 compression, 1 GB300)",
+                "value": rates[20] / 1e9, "unit": "G compressions/s",
+                "by_warps_per_sm": {str(k): v / 1e9 for k, v in rates.items()},
+                "alu_pipe_bound": alu_bound / 1e9, "frac_of_alu_pipe_bound": rates[20] / alu_bound,
+                "implied_digest_GBps": rates[20] * 1024 / 17 / 1e9,
+                "config": {"kernel": "compress_rate_kernel (blake3_selftest_compress_rate)",
+                           "iters_per_thread": iters, "threads_per_cta": 128,
+                           "implied": "16 leaf compressions + 1 parent per 1024-byte chunk"}}
     else:  # small: the 1 MiB digest, per call and replayed from a CUDA graph
         w = workloads.WORKLOADS["1MiB"]
         d = w.data(device="cuda")
@@ -733,7 +758,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--mode", choices=["headline", "xof", "stream", "small", "default"], default="headline")
+    ap.add_argument("--mode", choices=["headline", "xof", "stream", "small", "default", "ceiling"],
+                    default="headline")
     ap.add_argument("--xof-bytes", type=int, default=1 << 32)
     ap.add_argument("--segment-bytes", type=int, default=(256 << 20) + 777)
     args = ap.parse_args()

@@ -63,6 +63,7 @@ def library() -> ctypes.CDLL:
             "blake3_keyed_reduce_cvs": (i32, [vp, u64, vp, i32, i32, vp, vp, sz, vp]),
             "blake3_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32)]),
             "blake3_selftest_bounded_wait": (i32, [ctypes.c_uint32, ctypes.POINTER(ctypes.c_int)]),
+            "blake3_selftest_compress_rate": (i32, [ctypes.c_uint32, ctypes.c_uint32, vp, vp]),
             "blake3_keyed_hash_xof": (i32, [vp, u64, vp, vp, u64, vp]),
             "blake3_hasher_new": (i32, [vp, ctypes.POINTER(vp)]),
             "blake3_hasher_free": (None, [vp]),
@@ -263,6 +264,13 @@ def blake3_selftest_bounded_wait(limit_us: int) -> bool:
     flag = ctypes.c_int(-1)
     _check(library().blake3_selftest_bounded_wait(limit_us, ctypes.byref(flag)), "blake3_selftest_bounded_wait")
     return flag.value == 1
+
+
+def blake3_selftest_compress_rate(blocks: int, iters: int, sink: torch.Tensor, stream=None) -> None:
+    """Launch blocks x 128 threads of `iters` chained compressions each (no memory traffic
+    but the 4-byte `sink`), asynchronously on `stream`: the compression-only ceiling."""
+    _check(library().blake3_selftest_compress_rate(blocks, iters, _dev_ptr(sink, "sink"), _stream(stream)),
+           "blake3_selftest_compress_rate")
 
 
 def blake3_keyed_hash_xof(data: torch.Tensor, key, out_len: int, out: torch.Tensor | None = None,

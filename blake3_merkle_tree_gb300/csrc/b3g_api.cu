@@ -455,4 +455,11 @@ b3g_status blake3_selftest_bounded_wait(uint32_t limit_us, int *timed_out_out) {
     return st;
 }
 
+b3g_status blake3_selftest_compress_rate(uint32_t blocks, uint32_t iters, uint32_t *d_sink, b3g_stream_t stream) {
+    if (!d_sink) return B3G_ERR_NULL;
+    if (blocks < 1 || blocks > (1u << 20) || iters < 1 || iters > (1u << 20)) return B3G_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(d_sink) & 3u) return B3G_ERR_ALIGN;
+    return launch_compress_rate(blocks, iters, d_sink, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

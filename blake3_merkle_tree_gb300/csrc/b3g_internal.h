@@ -99,6 +99,8 @@ b3g_status launch_reduce(const ReduceArgs &args, cudaStream_t stream);
 
 // One-thread bounded-wait probe; writes 1 to *d_flag if the wait gave up.
 b3g_status launch_wait_probe(uint64_t limit_ns, int *d_flag, cudaStream_t stream);
+// `blocks` CTAs of 128 threads, each thread `iters` chained compressions, no memory traffic
+b3g_status launch_compress_rate(uint32_t blocks, uint32_t iters, uint32_t *d_sink, cudaStream_t stream);
 
 // Records a CUDA error for blake3_last_cuda_error() and returns B3G_ERR_CUDA.
 b3g_status cuda_fail(cudaError_t err, const char *what);

@@ -224,6 +224,20 @@ b3g_status blake3_device_status(uint32_t *status_out);
 b3g_status blake3_selftest_bounded_wait(uint32_t limit_us, int *timed_out_out);
 
 /*
+ * blake3_selftest_compress_rate -- launches `blocks` CTAs of 128 threads (1..2^20) on
+ * `stream`; every thread runs `iters` (1..2^20) chained keyed compressions with the
+ * same compression function as the hashing kernels, its 16 message words held in
+ * registers, and touches no memory but the 4-byte device word d_sink (written only on
+ * an impossible value).  blocks * 128 * iters compressions per launch: the
+ * compression-only ceiling, for the caller to time (asynchronous).  The compression
+ * is the one the page describes in its section "压缩函数" (7 rounds of G).
+ * Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_ALIGN (d_sink not 4-byte aligned),
+ * B3G_ERR_CUDA.
+ */
+b3g_status blake3_selftest_compress_rate(uint32_t blocks, uint32_t iters, uint32_t *d_sink,
+                                         b3g_stream_t stream);
+
+/*
  * blake3_keyed_hash_xof -- out_len bytes of extendable output for d_in[0..len) under
  * `key`, written to d_out (any alignment).  The first 32 bytes equal the digest of
  * blake3_keyed_hash.  Output block i (bytes 64i .. 64i+63) is the root compression

@@ -80,6 +80,16 @@ def test_sizes(lib):
     assert lib.blake3_reduce_workspace_size(32769, -1) == 33 * 32
 
 
+def test_compress_rate_selftest_checks_arguments_first(lib):
+    f = lib.blake3_selftest_compress_rate
+    f.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(1, 1, None, None) == 1  # no sink
+    assert f(0, 1, FAKE, None) == 6 and f(1, 0, FAKE, None) == 6  # empty launch
+    assert f((1 << 20) + 1, 1, FAKE, None) == 6 and f(1, (1 << 20) + 1, FAKE, None) == 6
+    assert f(1, 1, ctypes.c_void_p(0x10002), None) == 2  # sink not 4-byte aligned
+
+
 def test_argument_errors_before_any_cuda_call(lib):
     out = FAKE
     assert lib.blake3_keyed_hash(FAKE, 10, None, out, None) == 1
