@@ -1,6 +1,7 @@
 """The seeded input generators: torch (any device) == numpy == scalar restatement."""
 
 import numpy as np
+import pytest
 import torch
 
 from blake3_merkle_tree_gb300 import workloads
@@ -37,3 +38,18 @@ def test_workload_sizes():
     assert w["bf16_256MiB"].nbytes == 268_435_456
     small = workloads.bf16_matrix_bytes(2, rows=4, cols=8)
     assert small.dtype == torch.uint8 and small.numel() == 64
+
+
+def test_byte_ranges_of_a_stream_match_its_prefix():
+    """A slice [start, start + n) made on its own (start a multiple of 8) equals the same
+    bytes of the whole stream: what every rank of a sharded digest generates."""
+    import torch
+
+    w = workloads.WORKLOADS["12GiB+777"]
+    whole = workloads.uniform_bytes(w.data_seed, 3 << 20)
+    for start, n in [(0, 1000), (8, 4096), (128 * 1024, 777), ((1 << 20) + 16, 1 << 20)]:
+        assert torch.equal(w.data_range(start, n), whole[start:start + n])
+    with pytest.raises(ValueError):
+        workloads.uniform_bytes(6, 16, start=4)
+    with pytest.raises(ValueError):
+        workloads.WORKLOADS["bf16_256MiB"].data_range(0, 16)
