@@ -166,6 +166,23 @@ def _leaf_compressions(nbytes: int, tiles: int) -> int:
     return (nbytes // 1024) * 16 + ((tail + 63) // 64 if tail else 0) + (nchunks - tiles)
 
 
+def _sources_sha256() -> str:
+    """SHA-256 of the library's CUDA/C sources and the C header (first 16 hex digits): the
+    identity of the measured build, also where no version-control metadata travels."""
+    import hashlib
+
+    root = os.path.dirname(os.path.abspath(__file__))
+    csrc = os.path.join(root, "blake3_merkle_tree_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    files.append(os.path.join(root, "include", "blake3_gb300.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def _cpu_model() -> str:
     """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
     try:
@@ -410,7 +427,8 @@ def run_ours(args):
         "config": {"workload": f"{w.name} keyed BLAKE3, {w.kind} bytes seed {w.data_seed}, key seed {w.key_seed}",
                    "input": "u8 bytes, hashed as little-endian u32 words", "bytes": n, "chunks": nchunks,
                    "leaves_per_cta": 1 << leaves_log2, "cta_roots": tiles,
-                   "l2": f"input {n / 1e9:.2f} GB > 126 MB L2; no flush needed", "parallelism": "one GPU"},
+                   "l2": f"input {n / 1e9:.2f} GB > 126 MB L2; no flush needed", "parallelism": "one GPU",
+                   "sources_sha256": _sources_sha256()},
         "timing": timing, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches * args.steps, "clocks": clocks,
         "digest": digest_api.hex(),
@@ -523,7 +541,8 @@ def run_sharded(args, world, rank, local):
                    "bytes_this_rank": n_loc, "tiles": sd.tiles, "tiles_this_rank": n_tiles,
                    "l2": f"input {n_loc / 1e9:.2f} GB per GPU > 126 MB L2; no flush needed",
                    "parallelism": f"sharded{world}",
-                   "exchange": "all-gather of the 32-byte tile roots over NCCL, fold on every rank"},
+                   "exchange": "all-gather of the 32-byte tile roots over NCCL, fold on every rank",
+                   "sources_sha256": _sources_sha256()},
         "timing": timing, "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
         "gpu_launches": (int(n_tiles > 0) + _reduce_launches(sd.tiles)) * args.steps,
         "clocks": clk.summary(), "digest": digest.hex(),
