@@ -260,6 +260,149 @@ def _oracle_threaded(host_bytes: torch.Tensor, key: bytes, threads: int):
                       f"hashed in parallel by the unchanged oracle, folded on one thread ({dt:.1f} s)"}
 
 
+def _oracle_digest_threaded(host_bytes: torch.Tensor, key: bytes, threads: int) -> bytes:
+    """The oracle's digest of the whole input on all host cores: the tree is split the
+    way the specification splits it (left subtree = the largest power of two of chunks
+    below the count) until every piece holds at most 1/threads of the chunks; the pieces
+    are hashed in parallel by the unchanged oracle (oracle.subtree_cv, the ctypes call
+    releases the GIL), and the parents above them are folded on one thread with ROOT on
+    the top one."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+
+    n = host_bytes.numel()
+    nchunks = max(1, -(-n // 1024))
+    if nchunks == 1 or threads <= 1:
+        return oracle.keyed_hash(host_bytes, key)
+    per = max(1, -(-nchunks // threads))
+    leaves = []  # (first chunk, chunk count), left to right
+
+    def split(lo, cnt):
+        if cnt <= per:
+            leaves.append((lo, cnt))
+            return
+        left = 1 << ((cnt - 1).bit_length() - 1)
+        split(lo, left)
+        split(lo + left, cnt - left)
+
+    split(0, nchunks)
+    with ThreadPoolExecutor(threads) as ex:
+        cvs = dict(zip(leaves, ex.map(
+            lambda lc: oracle.subtree_cv(host_bytes[lc[0] * 1024:min(n, (lc[0] + lc[1]) * 1024)], key, lc[0]),
+            leaves)))
+
+    def fold(lo, cnt, root):
+        if (lo, cnt) in cvs:
+            return cvs[(lo, cnt)]
+        left = 1 << ((cnt - 1).bit_length() - 1)
+        return oracle.parent_cv(key, fold(lo, left, False), fold(lo + left, cnt - left, False), root)
+
+    return fold(0, nchunks, True)
+
+
+def _host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def _step_fn(lib, binding, dev, n, key, stream):
+    """One pass of the path over `dev`: the leaf launch (chunk CVs and CTA subtrees), then
+    the reduction launches to the ROOT digest.  Returns (step, digest tensor, launches)."""
+    sp = stream.cuda_stream
+    leaves_log2 = -1
+    tiles = lib.blake3_tile_count(n, leaves_log2)
+    roots = torch.empty((tiles, 32), dtype=torch.uint8, device="cuda")
+    red_ws = torch.empty(max(16, lib.blake3_reduce_workspace_size(tiles, -1)), dtype=torch.uint8, device="cuda")
+    out = torch.empty(32, dtype=torch.uint8, device="cuda")
+
+    def step(ev_a=None, ev_b=None):
+        if ev_a is not None:
+            ev_a.record(stream)
+        st = lib.blake3_keyed_tile_roots(dev.data_ptr(), n, 0, key, leaves_log2, 1, roots.data_ptr(), sp)
+        if st:
+            raise binding.B3GError(st, "blake3_keyed_tile_roots")
+        if ev_b is not None:
+            ev_b.record(stream)
+        if tiles > 1:
+            st = lib.blake3_keyed_reduce_cvs(roots.data_ptr(), tiles, key, 1, -1, out.data_ptr(), red_ws.data_ptr(),
+                                             red_ws.numel(), sp)
+            if st:
+                raise binding.B3GError(st, "blake3_keyed_reduce_cvs")
+
+    return step, (roots[0] if tiles == 1 else out), 1 + _reduce_launches(tiles), tiles
+
+
+def _roofline_fracs(n, tiles, leaf_s, hbm_peak, int_peak):
+    """The fractions of one leaf launch over n bytes: against the benchmark spec's roofline
+    (min(HBM peak, INT32 issue peak / the page's ops per byte), which is the HBM peak on
+    GB300), and against the issue peak with the plain instruction count."""
+    comps = _leaf_compressions(n, tiles)
+    page_bound = min(hbm_peak, int_peak / (comps * PAGE_OPS_PER_COMPRESSION / n) / 1e9)
+    gbs = n / leaf_s / 1e9
+    return {"leaf_GBps": gbs, "frac_of_min_roofline": gbs / page_bound, "min_roofline_GBps": page_bound,
+            "frac_hbm": gbs / hbm_peak,
+            "frac_issue_bound": comps * OPS_PER_COMPRESSION / leaf_s / int_peak}
+
+
+def _measure_config(lib, binding, wname, steps, hbm_peak, int_peak, threads):
+    """One configuration of the benchmark: GB/s of the leaf + reduction step (median of
+    per-step CUDA events; the L2 is flushed between steps when the input fits in it),
+    the roofline fractions of the leaf launch, and the digest against the oracle (on all
+    host cores)."""
+    w = workloads.WORKLOADS[wname]
+    key = w.key()
+    n = w.nbytes
+    dev = w.data(device="cuda")
+    stream = torch.cuda.current_stream()
+    step, digest_t, launches, tiles = _step_fn(lib, binding, dev, n, key, stream)
+    small = n < (256 << 20)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if small else None
+    for _ in range(3):
+        step()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b, c in evs:
+        if flush is not None:
+            flush.fill_(1)
+        step(a, b)
+        c.record(stream)
+    torch.cuda.synchronize()
+    step_ms = statistics.median(a.elapsed_time(c) for a, _, c in evs)
+    leaf_ms = statistics.median(a.elapsed_time(b) for a, b, _ in evs)
+    got = bytes(digest_t.cpu().numpy())
+    t0 = time.perf_counter()
+    ref = _oracle_digest_threaded(dev.cpu(), key, threads)
+    oracle_s = time.perf_counter() - t0
+    res = {"workload": f"{w.name} keyed BLAKE3, {w.kind} bytes seed {w.data_seed}, key seed {w.key_seed}",
+           "bytes": n, "steps": steps, "GBps": n / step_ms / 1e6, "ms_per_step": step_ms, "leaf_ms": leaf_ms,
+           "gpu_launches_per_step": launches,
+           "l2": "flushed between steps (256 MiB write)" if small else "input larger than L2",
+           "digest": got.hex(), "digest_equals_oracle": got == ref,
+           "oracle": f"unchanged oracle on {threads} host threads, {oracle_s:.1f} s"}
+    res.update(_roofline_fracs(n, tiles, leaf_ms / 1e3, hbm_peak, int_peak))
+    if not small:
+        res["l2_flush_needed"] = False
+    del dev, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def _ragged_config(binding):
+    """The ragged-length sweep (13 fixed and 64 seeded lengths): every digest through the
+    public call against the oracle."""
+    import oracle
+
+    lengths = workloads.ragged_lengths()
+    key = workloads.key_bytes(workloads.RAGGED_KEY_SEED)
+    bad = []
+    for length in lengths:
+        host = workloads.uniform_bytes(length, length)
+        got = bytes(binding.blake3_keyed_hash(host.to("cuda"), key).cpu().numpy())
+        if got != oracle.keyed_hash(host, key):
+            bad.append(length)
+    return {"workload": "ragged-length sweep: 13 fixed + 64 seeded lengths in [1, 4 MiB], seed = length, key seed 1",
+            "lengths": len(lengths), "digests_equal_oracle": len(lengths) - len(bad), "mismatched_lengths": bad}
+
+
 def run_reference(args):
     """Reference arm: the CPU oracle, timed on the host cores, on bounded prefixes."""
     world, rank, _ = _dist()
@@ -389,9 +532,19 @@ def run_ours(args):
                        "frac": page_ops / leaf_s / int_peak},
         "hbm": {"achieved": n / leaf_s / 1e9, "peak": float(peaks.get("hbm_gbs", 6800.0)), "unit": "GB/s",
                 "frac": n / leaf_s / 1e9 / float(peaks.get("hbm_gbs", 6800.0)), "peak_kind": peak_kind},
-        "roofline_gbs": min(float(peaks.get("hbm_gbs", 6800.0)), int_peak / (ops / n) / 1e9),
+        "issue_bound_GBps": int_peak / (ops / n) / 1e9,
     }
-    roofline["frac_of_min_roofline"] = (n / leaf_s / 1e9) / roofline["roofline_gbs"]
+    # the benchmark spec's roofline: the slower of the input bytes at the HBM peak and the page's
+    # integer operations per byte at the INT32 issue peak (the HBM peak on GB300)
+    fr = _roofline_fracs(n, tiles, leaf_s, float(peaks.get("hbm_gbs", 6800.0)), int_peak)
+    roofline["roofline_gbs"] = fr["min_roofline_GBps"]
+    roofline["frac_of_min_roofline"] = fr["frac_of_min_roofline"]
+    roofline["frac_issue_bound"] = fr["frac_issue_bound"]
+    roofline["definitions"] = {
+        "frac": "680 integer instructions per compression (the plain count) / the INT32 issue peak",
+        "frac_of_min_roofline": "input bytes / min(HBM peak, INT32 issue peak / the page's 336 ops per block) "
+                                "(north_star's definition; the HBM peak on this GPU)",
+        "frac_issue_bound": "same as frac"}
     traffic, traffic_src, issued = _traffic_per_launch(lib, nchunks)
     roofline["traffic"] = traffic
     roofline["traffic_source"] = traffic_src
@@ -420,6 +573,30 @@ def run_ours(args):
         if cores > 1:
             cpu["all_cores"] = _oracle_threaded(host, key, cores)
 
+    # the headline digest against the oracle, on all host cores
+    digest_oracle = None
+    if not args.no_oracle_check:
+        if host is None:
+            host = dev.cpu()
+        t0 = time.perf_counter()
+        ok = _oracle_digest_threaded(host, key, _host_cores()) == digest_api
+        digest_oracle = {"equal": ok, "threads": _host_cores(), "seconds": round(time.perf_counter() - t0, 1)}
+    del host
+
+    # the other configurations of the workload set, each with its own GB/s, roofline
+    # fractions and oracle check (C5, the largest, is the headline above)
+    configs = None
+    if not args.no_configs:
+        hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+        th = _host_cores()
+        configs = {
+            "C1_1MiB": _measure_config(lib, binding, "1MiB", 200, hbm_peak, int_peak, th),
+            "C2_ragged": _ragged_config(binding),
+            "C3_bf16_256MiB": _measure_config(lib, binding, "bf16_256MiB", 50, hbm_peak, int_peak, th),
+            "C4_4GiB": _measure_config(lib, binding, "4GiB", 20, hbm_peak, int_peak, th),
+        }
+        configs["C4_4GiB"]["target"] = "frac_issue_bound >= 0.70 (north_star: >= 70 % of the roofline for >= 4 GiB)"
+
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -431,7 +608,7 @@ def run_ours(args):
                    "sources_sha256": _sources_sha256()},
         "timing": timing, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches * args.steps, "clocks": clocks,
-        "digest": digest_api.hex(),
+        "digest": digest_api.hex(), "digest_vs_oracle": digest_oracle, "configs": configs,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -721,6 +898,44 @@ def run_mode(args):
                 "config": {"kernel": "compress_rate_kernel (blake3_selftest_compress_rate)",
                            "iters_per_thread": iters, "threads_per_cta": 128,
                            "implied": "16 leaf compressions + 1 parent per 1024-byte chunk"}}
+    elif args.mode == "latency":
+        # several lanes per chunk (the page's future-work item): the latency of a chain of
+        # dependent compressions in one warp, one lane per chain against four lanes per
+        # chain (the state split by columns, shuffles for the diagonal step)
+        key = workloads.key_bytes(11)
+        peaks, _ = _peaks()
+        mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        res = {}
+        for lanes in (1, 4):
+            cvs = torch.zeros((32 // lanes, 32), dtype=torch.uint8, device="cuda")
+            cycles = torch.zeros(1, dtype=torch.int64, device="cuda")
+            per = {}
+            for chain in (16, 1024):
+                for _ in range(args.warmup):
+                    binding.blake3_selftest_compress_latency(lanes, chain, key, cvs, cycles)
+                torch.cuda.synchronize()
+                cyc = []
+                for _ in range(args.steps):
+                    binding.blake3_selftest_compress_latency(lanes, chain, key, cvs, cycles)
+                    torch.cuda.synchronize()
+                    cyc.append(int(cycles.item()))
+                c = statistics.median(cyc)
+                per[str(chain)] = {"cycles": c, "cycles_per_compression": c / chain,
+                                   "us_at_max_clock": c / mhz}
+            ms16 = _timed(lambda: binding.blake3_selftest_compress_latency(lanes, 16, key, cvs, cycles),
+                          args.steps, args.warmup)
+            res[f"{lanes}_lane{'s' if lanes > 1 else ''}_per_chunk"] = {
+                "chains_per_warp": 32 // lanes, "by_chain": per, "launch_us_chain16_events": ms16 * 1e3}
+        one = res["1_lane_per_chunk"]["by_chain"]["1024"]["cycles_per_compression"]
+        four = res["4_lanes_per_chunk"]["by_chain"]["1024"]["cycles_per_compression"]
+        line = {"mode": "latency", "metric": "cycles per dependent compression, one warp (keyed BLAKE3, 1 GB300)",
+                "value": four / one, "unit": "4-lane latency / 1-lane latency", "results": res,
+                "config": {"kernel": "compress_latency_kernel (blake3_selftest_compress_latency)",
+                           "clock_for_us": f"{mhz:.0f} MHz (maximum SM clock)",
+                           "chunk_latency_16_blocks_us": {"1 lane": res["1_lane_per_chunk"]["by_chain"]["16"]
+                                                          ["us_at_max_clock"],
+                                                          "4 lanes": res["4_lanes_per_chunk"]["by_chain"]["16"]
+                                                          ["us_at_max_clock"]}}}
     else:  # small: the 1 MiB digest, per call and replayed from a CUDA graph
         w = workloads.WORKLOADS["1MiB"]
         d = w.data(device="cuda")
@@ -776,8 +991,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration measurements")
+    ap.add_argument("--no-oracle-check", action="store_true", help="skip the oracle check of the headline digest")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--mode", choices=["headline", "xof", "stream", "small", "default", "ceiling"],
+    ap.add_argument("--mode", choices=["headline", "xof", "stream", "small", "default", "ceiling", "latency"],
                     default="headline")
     ap.add_argument("--xof-bytes", type=int, default=1 << 32)
     ap.add_argument("--segment-bytes", type=int, default=(256 << 20) + 777)

@@ -55,6 +55,9 @@ def library() -> ctypes.CDLL:
             "blake3_workspace_size": (sz, [u64]),
             "blake3_keyed_hash_ws": (i32, [vp, u64, vp, vp, vp, sz, vp]),
             "blake3_keyed_hash_noalloc": (i32, [vp, u64, vp, vp, vp]),
+            "blake3_keyed_hash_ex": (i32, [vp, u64, vp, vp, vp, sz, vp, vp]),
+            "blake3_selftest_bounded_wait_ex": (i32, [ctypes.c_uint32, vp, vp]),
+            "blake3_selftest_compress_latency": (i32, [i32, ctypes.c_uint32, vp, vp, vp, vp]),
             "blake3_keyed_chunk_cvs": (i32, [vp, u64, u64, vp, vp, vp]),
             "blake3_keyed_subtree_root": (i32, [vp, u64, u64, vp, i32, vp, vp]),
             "blake3_tile_count": (u64, [u64, i32]),
@@ -166,6 +169,19 @@ def blake3_keyed_hash_ws(data: torch.Tensor, key, workspace: torch.Tensor | None
     return out
 
 
+def blake3_keyed_hash_ex(data: torch.Tensor, key, status: torch.Tensor, workspace: torch.Tensor | None = None,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Keyed digest whose kernels report a given-up wait in `status` (a CUDA int32/uint32
+    word the caller owns and zeroes), in stream order."""
+    out = _out32(out, data)
+    ws_ptr = _dev_ptr(workspace, "workspace") if workspace is not None else None
+    ws_bytes = _nbytes(workspace) if workspace is not None else 0
+    st = library().blake3_keyed_hash_ex(_dev_ptr(data, "data"), _nbytes(data), _key(key), _dev_ptr(out, "out"),
+                                        ws_ptr, ws_bytes, _dev_ptr(status, "status"), _stream(stream))
+    _check(st, "blake3_keyed_hash_ex")
+    return out
+
+
 def blake3_hash(data: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Default-mode (unkeyed) digest of the contiguous CUDA tensor `data`."""
     out = _out32(out, data)
@@ -264,6 +280,22 @@ def blake3_selftest_bounded_wait(limit_us: int) -> bool:
     flag = ctypes.c_int(-1)
     _check(library().blake3_selftest_bounded_wait(limit_us, ctypes.byref(flag)), "blake3_selftest_bounded_wait")
     return flag.value == 1
+
+
+def blake3_selftest_bounded_wait_ex(limit_us: int, status: torch.Tensor, stream=None) -> None:
+    """The bounded-wait probe on `stream`, ORing the timeout bit into the device word `status`."""
+    _check(library().blake3_selftest_bounded_wait_ex(limit_us, _dev_ptr(status, "status"), _stream(stream)),
+           "blake3_selftest_bounded_wait_ex")
+
+
+def blake3_selftest_compress_latency(lanes_per_chunk: int, chain: int, key, cvs: torch.Tensor,
+                                     cycles: torch.Tensor, stream=None) -> None:
+    """One warp of compression chains with 1 or 4 lanes per chain (asynchronous): the chains'
+    final CVs into `cvs` (32 / lanes_per_chunk x 32 bytes) and lane 0's cycles into `cycles`
+    (an int64 CUDA tensor)."""
+    _check(library().blake3_selftest_compress_latency(lanes_per_chunk, chain, _key(key), _dev_ptr(cvs, "cvs"),
+                                                      _dev_ptr(cycles, "cycles"), _stream(stream)),
+           "blake3_selftest_compress_latency")
 
 
 def blake3_selftest_compress_rate(blocks: int, iters: int, sink: torch.Tensor, stream=None) -> None:

@@ -156,10 +156,14 @@ bool fused_path(const void *d_in, uint64_t n_full) {
 
 // The whole path: leaf kernel, then the reduction levels.  `ws` must hold
 // blake3_workspace_size(len) bytes when more than one tile exists.
+// `call_status`: a caller's device word that the kernels of this call report a
+// given-up wait in, instead of the per-device status word (NULL: the device word).
 b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
-                      uint32_t mode_flags, bool root, uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
-    uint32_t *status = nullptr;
-    b3g_status st = status_word(&status);
+                      uint32_t mode_flags, bool root, uint8_t *d_out32, uint8_t *ws, cudaStream_t stream,
+                      uint32_t *call_status = nullptr) {
+    uint32_t *status = call_status;
+    b3g_status st = B3G_OK;
+    if (!status) st = status_word(&status);
     if (st != B3G_OK) return st;
     const int t = choose_leaves_log2(n_chunks_of(len));
     LeafArgs a = leaf_args(d_in, len, chunk_offset, key, mode_flags, t, root, nullptr, status);
@@ -194,15 +198,16 @@ size_t hash_workspace(uint64_t len) {
 
 // Runs hash_range with a stream-ordered temporary workspace.
 b3g_status hash_range_alloc(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
-                            uint32_t mode_flags, bool root, uint8_t *d_out32, cudaStream_t stream) {
+                            uint32_t mode_flags, bool root, uint8_t *d_out32, cudaStream_t stream,
+                            uint32_t *call_status = nullptr) {
     const size_t need = hash_workspace(len);
     void *ws = nullptr;
     if (need) {
         cudaError_t e = alloc_async(&ws, need, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
     }
-    b3g_status st =
-        hash_range(d_in, len, chunk_offset, key, mode_flags, root, d_out32, static_cast<uint8_t *>(ws), stream);
+    b3g_status st = hash_range(d_in, len, chunk_offset, key, mode_flags, root, d_out32, static_cast<uint8_t *>(ws),
+                               stream, call_status);
     if (ws) {
         cudaError_t e = cudaFreeAsync(ws, stream);
         if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
@@ -213,6 +218,8 @@ b3g_status hash_range_alloc(const void *d_in, uint64_t len, uint64_t chunk_offse
 }  // namespace
 
 b3g_status device_status_word(uint32_t **out) { return status_word(out); }
+
+int leaves_log2_for(uint64_t n_chunks) { return choose_leaves_log2(n_chunks); }
 
 b3g_status hash_range_ws(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
                          uint32_t mode_flags, bool root, uint8_t *d_out32, uint8_t *ws, cudaStream_t stream) {
@@ -328,6 +335,20 @@ b3g_status blake3_keyed_hash_ws(const void *d_in, uint64_t len, const uint8_t ke
     }
     return hash_range(d_in, len, 0, key, kModeKeyed, true, d_out32, static_cast<uint8_t *>(d_ws),
                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+b3g_status blake3_keyed_hash_ex(const void *d_in, uint64_t len, const uint8_t key[32], uint8_t *d_out32,
+                                void *d_ws, size_t ws_bytes, uint32_t *d_status, b3g_stream_t stream) {
+    if (!key || !d_out32 || !d_status || (!d_in && len > 0)) return B3G_ERR_NULL;
+    if (misaligned16(d_out32) || (reinterpret_cast<uintptr_t>(d_status) & 3u)) return B3G_ERR_ALIGN;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!d_ws) return hash_range_alloc(d_in, len, 0, key, kModeKeyed, true, d_out32, s, d_status);
+    const size_t need = hash_workspace(len);
+    if (need) {
+        if (ws_bytes < need) return B3G_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(d_ws) & 15u) return B3G_ERR_ALIGN;
+    }
+    return hash_range(d_in, len, 0, key, kModeKeyed, true, d_out32, static_cast<uint8_t *>(d_ws), s, d_status);
 }
 
 b3g_status blake3_hash(const void *d_in, uint64_t len, uint8_t *d_out32, b3g_stream_t stream) {
@@ -453,6 +474,26 @@ b3g_status blake3_selftest_bounded_wait(uint32_t limit_us, int *timed_out_out) {
     cudaFree(d_flag);
     if (st == B3G_OK) *timed_out_out = h;
     return st;
+}
+
+b3g_status blake3_selftest_bounded_wait_ex(uint32_t limit_us, uint32_t *d_status, b3g_stream_t stream) {
+    if (!d_status) return B3G_ERR_NULL;
+    if (limit_us < 1 || limit_us > 10000000u) return B3G_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(d_status) & 3u) return B3G_ERR_ALIGN;
+    return launch_wait_probe_status(static_cast<uint64_t>(limit_us) * 1000ull, d_status,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+b3g_status blake3_selftest_compress_latency(int lanes_per_chunk, uint32_t chain, const uint8_t key[32],
+                                            uint8_t *d_cvs, uint64_t *d_cycles, b3g_stream_t stream) {
+    if (!key || !d_cvs || !d_cycles) return B3G_ERR_NULL;
+    if ((lanes_per_chunk != 1 && lanes_per_chunk != 4) || chain < 1 || chain > (1u << 20)) return B3G_ERR_ARG;
+    if (misaligned16(d_cvs) || (reinterpret_cast<uintptr_t>(d_cycles) & 7u)) return B3G_ERR_ALIGN;
+    LatencyArgs a;
+    key_words(key, a.key);
+    a.out = d_cvs;
+    a.cycles = reinterpret_cast<unsigned long long *>(d_cycles);
+    return launch_compress_latency(lanes_per_chunk, chain, a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 b3g_status blake3_selftest_compress_rate(uint32_t blocks, uint32_t iters, uint32_t *d_sink, b3g_stream_t stream) {

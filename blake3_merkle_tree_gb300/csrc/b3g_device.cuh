@@ -260,6 +260,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (cached in L2 only), tracked per thread in
+// copy groups; the L2 fetches the whole 256-byte segment around it, so the next blocks
+// of the same chunk are L2 hits.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Closes this thread's current copy group (an empty group if it issued no copy).
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's copy groups are still in flight.  The copies
+// of the completed groups are then visible to this thread; a barrier makes them
+// visible to the others.  A hardware wait for the thread's own copies, not a spin.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Orders this thread's earlier generic-proxy shared-memory accesses before its later
 // async-proxy ones (a bulk copy into a stage the warp has just read).
 __device__ __forceinline__ void fence_proxy_async_smem() {

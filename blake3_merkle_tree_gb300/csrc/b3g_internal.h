@@ -99,8 +99,19 @@ b3g_status launch_reduce(const ReduceArgs &args, cudaStream_t stream);
 
 // One-thread bounded-wait probe; writes 1 to *d_flag if the wait gave up.
 b3g_status launch_wait_probe(uint64_t limit_ns, int *d_flag, cudaStream_t stream);
+// The same probe, ORing B3G_DEVICE_STATUS_TIMEOUT into *d_status (stream ordered) if the wait gave up.
+b3g_status launch_wait_probe_status(uint64_t limit_ns, uint32_t *d_status, cudaStream_t stream);
 // `blocks` CTAs of 128 threads, each thread `iters` chained compressions, no memory traffic
 b3g_status launch_compress_rate(uint32_t blocks, uint32_t iters, uint32_t *d_sink, cudaStream_t stream);
+
+// Arguments of the compression-latency self-test (several lanes per chunk).
+struct LatencyArgs {
+    uint32_t key[8];
+    uint8_t *out;                // 32 / lanes CVs of 32 bytes
+    unsigned long long *cycles;  // clock cycles of the whole chain (lane 0)
+};
+// One warp: chains of `chain` dependent compressions with 1 or 4 lanes per chain.
+b3g_status launch_compress_latency(int lanes, uint32_t chain, const LatencyArgs &a, cudaStream_t stream);
 
 // Records a CUDA error for blake3_last_cuda_error() and returns B3G_ERR_CUDA.
 b3g_status cuda_fail(cudaError_t err, const char *what);
@@ -132,6 +143,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
+
+// CTA subtree size (log2 of the chunks) the one-shot digest uses for n chunks: 128
+// chunks, fewer (down to 32) for inputs of at most 2^16 chunks so that at least one
+// CTA per SM exists.
+int leaves_log2_for(uint64_t n_chunks);
 
 // Device address of the current device's status word (looked up once per device).
 b3g_status device_status_word(uint32_t **out);

@@ -98,17 +98,18 @@ constexpr uint32_t kBarTree = 1;  // named barrier id of the consumer threads
 //   LOAD       bytes of every chunk brought by one copy (128 or 64)
 //   CHUNK_CVS  write every chunk CV instead of reducing the tile (no reducer work)
 // ---------------------------------------------------------------------------------
-template <int C, int S, int LOAD, bool CHUNK_CVS>
+template <int C, int S, int LOAD, bool CHUNK_CVS, uint32_t STAGE = 32 * LOAD>
 struct TmaCfg {
     static_assert(C % 32 == 0 && C >= 32 && C <= 256, "consumer count");
     static_assert(LOAD == 128 || LOAD == 64, "load width");
+    static constexpr int kC = C;
     static constexpr int kLoadsPerChunk = 1024 / LOAD;
     static constexpr int kBlocksPerLoad = LOAD / 64;
     static constexpr int kConsumerWarps = C / 32;
     static constexpr int kReducerWarp = kConsumerWarps;
     static constexpr int kThreads = C + 32;
     static constexpr uint32_t kRowsPerCopy = 32;                    // one warp's rows
-    static constexpr uint32_t kStageBytes = kRowsPerCopy * LOAD;  // = the copy's box bytes
+    static constexpr uint32_t kStageBytes = STAGE;  // the bulk tensor copy's box bytes: 32 rows x LOAD
     static constexpr uint32_t kRingBytes = S * kStageBytes;
     static constexpr uint32_t kNodeBytes = C * 32;            // one node buffer
     static constexpr uint32_t kScratch1Bytes = (C / 2) * 32;  // odd tree levels
@@ -207,6 +208,153 @@ __device__ __forceinline__ void fused_final_reduce(const LeafArgs &a, const uint
     }
 }
 
+// The reducer warp of the leaf kernels (page sections "Merkle Tree 归约" and "未来工作"):
+// turns each tile's chunk CVs, handed over in node buffer k & 1, into the tile CV.
+template <typename Cfg, uint32_t MODE>
+__device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t key[8], uint32_t rings0,
+                                             uint32_t nodes0, uint32_t cvfull0, uint32_t cvempty0) {
+    constexpr int C = Cfg::kC;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t scratch1 = rings0 + Cfg::kOffScratch1;
+    const uint32_t scratch2 = rings0 + Cfg::kOffScratch2;
+
+    const uint32_t topA = rings0 + Cfg::kOffTopA;
+    const uint32_t topB = rings0 + Cfg::kOffTopB;
+    Words8 key8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) key8.w[i] = key[i];
+    // Full tiles are reduced down to 32 nodes each, which wait side by side in
+    // top A; every kTopBatch tiles the top levels of all of them run as one
+    // array (pairing never mixes two tiles: each holds a power-of-two count),
+    // so those levels keep whole warps busy instead of 16, 8, 4, 2 and 1 lanes.
+    uint32_t pending = 0;  // tiles waiting in top A
+    uint64_t first = 0;    // the first of them (the others follow at gridDim.x)
+    auto flush = [&]() {
+        if (pending == 0) return;
+        uint32_t n = pending * 32u, src = topA, dst = topB;
+        while (n > pending) {
+            pair_level(src, dst, n >> 1, key8, MODE);
+            __syncwarp();
+            const uint32_t t = src;
+            src = dst;
+            dst = t;
+            n >>= 1;
+        }
+        if (lane < pending) {
+            uint32_t x[8];
+            load_node(src, lane, x);
+            uint4 *o = reinterpret_cast<uint4 *>(a.out + (first + static_cast<uint64_t>(lane) * gridDim.x) * 32);
+            o[0] = make_uint4(x[0], x[1], x[2], x[3]);
+            o[1] = make_uint4(x[4], x[5], x[6], x[7]);
+        }
+        __syncwarp();
+        pending = 0;
+    };
+    uint32_t k = 0;
+    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
+        const uint32_t b = k & 1u;
+        const uint32_t src0 = nodes0 + b * Cfg::kNodeBytes;
+        if (!mbar_wait_bounded(cvfull0 + 8 * b, (k >> 1) & 1u, a.wait_limit_ns)) {
+            atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
+            break;
+        }
+        const uint64_t rem = a.n_chunks - tile * C;
+        uint32_t cnt = rem < C ? static_cast<uint32_t>(rem) : static_cast<uint32_t>(C);
+        if (Cfg::kTopBatch > 0 && cnt == C && !a.ticket && !(a.root && a.n_tiles == 1)) {
+            // a full tile: its levels down to 32 nodes, the last into top A
+            const uint32_t slot = topA + pending * 1024u;
+            uint32_t src = src0, level = 0;
+            for (uint32_t n = C; n > 32; n >>= 1, ++level) {
+                const uint32_t dst = n == 64 ? slot : ((level & 1u) ? scratch2 : scratch1);
+                pair_level(src, dst, n >> 1, key8, MODE);
+                __syncwarp();
+                if (level == 0) mbar_arrive(cvempty0 + 8 * b);  // node buffer read
+                src = dst;
+            }
+            if (level == 0) {  // 32 chunks per tile: the node buffer is the top level
+                uint32_t x[8];
+                load_node(src0, lane, x);
+                __syncwarp();
+                mbar_arrive(cvempty0 + 8 * b);
+                store_node(slot, lane, x);
+                __syncwarp();
+            }
+            if (pending == 0) first = tile;
+            if (++pending == Cfg::kTopBatch) flush();
+            continue;
+        }
+        // a partial tile, a single-tile root or the fused final reduction: on its own
+        flush();
+        uint32_t src = src0;
+        uint32_t level = 0;
+        // Levels with more than 32 nodes: pairs (2j, 2j+1) -> node j,
+        // ping-ponging between two scratch buffers; an odd last node moves up
+        // unchanged.
+        while (cnt > 32) {
+            const uint32_t dst = (level & 1u) ? scratch2 : scratch1;
+            const uint32_t half = cnt >> 1;
+            pair_level(src, dst, half, key8, MODE);
+            if ((cnt & 1u) && lane == 0) {
+                uint32_t t[8];
+                load_node(src, cnt - 1, t);
+                store_node(dst, half, t);
+            }
+            __syncwarp();
+            if (level == 0) mbar_arrive(cvempty0 + 8 * b);  // node buffer read
+            src = dst;
+            cnt = (cnt + 1) >> 1;
+            ++level;
+        }
+        uint32_t x[8];
+        if (lane < cnt) load_node(src, lane, x);
+        __syncwarp();
+        if (level == 0) mbar_arrive(cvempty0 + 8 * b);
+        warp_tree(x, cnt, key, MODE, a.root && a.n_tiles == 1);
+        if (lane == 0) {
+            uint4 *o = reinterpret_cast<uint4 *>(a.out + tile * 32);
+            o[0] = make_uint4(x[0], x[1], x[2], x[3]);
+            o[1] = make_uint4(x[4], x[5], x[6], x[7]);
+        }
+        if (a.ticket) fused_final_reduce(a, key, MODE);
+    }
+    flush();
+}
+
+// End of a consumer thread's tile: the owner of the partial last chunk redoes it from
+// global memory (its row in the stage was not that chunk's bytes), then the chunk CV is
+// written out (CHUNK_CVS) or handed to the reducer: wait until node buffer k & 1 is free
+// (the reducer has read tile k - 2), store, arrive.  Returns false if that wait gave up.
+template <typename Cfg, bool CHUNK_CVS, uint32_t MODE>
+__device__ __forceinline__ bool finish_tile(const LeafArgs &a, const uint32_t key[8], uint32_t cv[8],
+                                            uint64_t chunk, uint64_t ctr, uint32_t end_flags, uint32_t k,
+                                            uint32_t nodes0, uint32_t cvfull0, uint32_t cvempty0) {
+    const bool valid = chunk < a.n_chunks;
+    if (a.tail_bytes != 0 && chunk == a.n_full) {
+        Words8 k8, t;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) k8.w[i] = key[i];
+        t = partial_chunk_cv(a.in, a.len, chunk * kChunkBytes, ctr, a.tail_bytes, MODE | end_flags, k8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cv[i] = t.w[i];
+    }
+    if constexpr (CHUNK_CVS) {
+        if (valid) {
+            uint4 *o = reinterpret_cast<uint4 *>(a.out + chunk * 32);
+            o[0] = make_uint4(cv[0], cv[1], cv[2], cv[3]);
+            o[1] = make_uint4(cv[4], cv[5], cv[6], cv[7]);
+        }
+    } else {
+        const uint32_t b = k & 1u;
+        if (k >= 2 && !mbar_wait_bounded(cvempty0 + 8 * b, ((k >> 1) - 1) & 1u, a.wait_limit_ns)) {
+            atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
+            return false;
+        }
+        if (valid) store_node(nodes0 + b * Cfg::kNodeBytes, threadIdx.x, cv);
+        mbar_arrive(cvfull0 + 8 * b);
+    }
+    return true;
+}
+
 template <int C, int S, int LOAD, bool CHUNK_CVS, uint32_t MODE>
 __global__ void B3G_LEAF_BOUNDS(C + 32)
     leaf_tma_kernel(const __grid_constant__ CUtensorMap tmap, const LeafArgs a) {
@@ -215,8 +363,6 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t rings0 = (raw + 1023u) & ~1023u;
     const uint32_t nodes0 = rings0 + Cfg::kOffNodes;  // buffer b at nodes0 + b * kNodeBytes
-    const uint32_t scratch1 = rings0 + Cfg::kOffScratch1;
-    const uint32_t scratch2 = rings0 + Cfg::kOffScratch2;
     const uint32_t full0 = rings0 + Cfg::kOffBars;               // S barriers per consumer warp
     const uint32_t cvfull0 = full0 + 8 * Cfg::kConsumerWarps * S;  // 2: node buffer b is filled
     const uint32_t cvempty0 = cvfull0 + 16;                        // 2: node buffer b is free
@@ -247,108 +393,7 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
 
     if (warp == Cfg::kReducerWarp) {
         // -------------------------------- reducer --------------------------------
-        if constexpr (!CHUNK_CVS) {
-            const uint32_t topA = rings0 + Cfg::kOffTopA;
-            const uint32_t topB = rings0 + Cfg::kOffTopB;
-            Words8 key8;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) key8.w[i] = key[i];
-            // Full tiles are reduced down to 32 nodes each, which wait side by side in
-            // top A; every kTopBatch tiles the top levels of all of them run as one
-            // array (pairing never mixes two tiles: each holds a power-of-two count),
-            // so those levels keep whole warps busy instead of 16, 8, 4, 2 and 1 lanes.
-            uint32_t pending = 0;  // tiles waiting in top A
-            uint64_t first = 0;    // the first of them (the others follow at gridDim.x)
-            auto flush = [&]() {
-                if (pending == 0) return;
-                uint32_t n = pending * 32u, src = topA, dst = topB;
-                while (n > pending) {
-                    pair_level(src, dst, n >> 1, key8, MODE);
-                    __syncwarp();
-                    const uint32_t t = src;
-                    src = dst;
-                    dst = t;
-                    n >>= 1;
-                }
-                if (lane < pending) {
-                    uint32_t x[8];
-                    load_node(src, lane, x);
-                    uint4 *o = reinterpret_cast<uint4 *>(a.out + (first + static_cast<uint64_t>(lane) * gridDim.x) * 32);
-                    o[0] = make_uint4(x[0], x[1], x[2], x[3]);
-                    o[1] = make_uint4(x[4], x[5], x[6], x[7]);
-                }
-                __syncwarp();
-                pending = 0;
-            };
-            uint32_t k = 0;
-            for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
-                const uint32_t b = k & 1u;
-                const uint32_t src0 = nodes0 + b * Cfg::kNodeBytes;
-                if (!mbar_wait_bounded(cvfull0 + 8 * b, (k >> 1) & 1u, a.wait_limit_ns)) {
-                    atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
-                    break;
-                }
-                const uint64_t rem = a.n_chunks - tile * C;
-                uint32_t cnt = rem < C ? static_cast<uint32_t>(rem) : static_cast<uint32_t>(C);
-                if (Cfg::kTopBatch > 0 && cnt == C && !a.ticket && !(a.root && a.n_tiles == 1)) {
-                    // a full tile: its levels down to 32 nodes, the last into top A
-                    const uint32_t slot = topA + pending * 1024u;
-                    uint32_t src = src0, level = 0;
-                    for (uint32_t n = C; n > 32; n >>= 1, ++level) {
-                        const uint32_t dst = n == 64 ? slot : ((level & 1u) ? scratch2 : scratch1);
-                        pair_level(src, dst, n >> 1, key8, MODE);
-                        __syncwarp();
-                        if (level == 0) mbar_arrive(cvempty0 + 8 * b);  // node buffer read
-                        src = dst;
-                    }
-                    if (level == 0) {  // 32 chunks per tile: the node buffer is the top level
-                        uint32_t x[8];
-                        load_node(src0, lane, x);
-                        __syncwarp();
-                        mbar_arrive(cvempty0 + 8 * b);
-                        store_node(slot, lane, x);
-                        __syncwarp();
-                    }
-                    if (pending == 0) first = tile;
-                    if (++pending == Cfg::kTopBatch) flush();
-                    continue;
-                }
-                // a partial tile, a single-tile root or the fused final reduction: on its own
-                flush();
-                uint32_t src = src0;
-                uint32_t level = 0;
-                // Levels with more than 32 nodes: pairs (2j, 2j+1) -> node j,
-                // ping-ponging between two scratch buffers; an odd last node moves up
-                // unchanged.
-                while (cnt > 32) {
-                    const uint32_t dst = (level & 1u) ? scratch2 : scratch1;
-                    const uint32_t half = cnt >> 1;
-                    pair_level(src, dst, half, key8, MODE);
-                    if ((cnt & 1u) && lane == 0) {
-                        uint32_t t[8];
-                        load_node(src, cnt - 1, t);
-                        store_node(dst, half, t);
-                    }
-                    __syncwarp();
-                    if (level == 0) mbar_arrive(cvempty0 + 8 * b);  // node buffer read
-                    src = dst;
-                    cnt = (cnt + 1) >> 1;
-                    ++level;
-                }
-                uint32_t x[8];
-                if (lane < cnt) load_node(src, lane, x);
-                __syncwarp();
-                if (level == 0) mbar_arrive(cvempty0 + 8 * b);
-                warp_tree(x, cnt, key, MODE, a.root && a.n_tiles == 1);
-                if (lane == 0) {
-                    uint4 *o = reinterpret_cast<uint4 *>(a.out + tile * 32);
-                    o[0] = make_uint4(x[0], x[1], x[2], x[3]);
-                    o[1] = make_uint4(x[4], x[5], x[6], x[7]);
-                }
-                if (a.ticket) fused_final_reduce(a, key, MODE);
-            }
-            flush();
-        }
+        if constexpr (!CHUNK_CVS) reducer_warp<Cfg, MODE>(a, key, rings0, nodes0, cvfull0, cvempty0);
         return;
     }
 
@@ -451,32 +496,9 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
             }
         }
         if (aborted) break;
-        if (a.tail_bytes != 0 && chunk == a.n_full) {
-            Words8 k8, t;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) k8.w[i] = key[i];
-            t = partial_chunk_cv(a.in, a.len, chunk * kChunkBytes, ctr, a.tail_bytes, MODE | end_flags, k8);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) cv[i] = t.w[i];
-        }
-
-        if constexpr (CHUNK_CVS) {
-            if (valid) {
-                uint4 *o = reinterpret_cast<uint4 *>(a.out + chunk * 32);
-                o[0] = make_uint4(cv[0], cv[1], cv[2], cv[3]);
-                o[1] = make_uint4(cv[4], cv[5], cv[6], cv[7]);
-            }
-        } else {
-            // hand the chunk CV to the reducer: wait until node buffer k&1 is free
-            // (the reducer has read tile k-2), store, arrive
-            const uint32_t b = k & 1u;
-            if (k >= 2 && !mbar_wait_bounded(cvempty0 + 8 * b, ((k >> 1) - 1) & 1u, a.wait_limit_ns)) {
-                atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
-                aborted = true;
-                break;
-            }
-            if (valid) store_node(nodes0 + b * Cfg::kNodeBytes, r, cv);
-            mbar_arrive(cvfull0 + 8 * b);
+        if (!finish_tile<Cfg, CHUNK_CVS, MODE>(a, key, cv, chunk, ctr, end_flags, k, nodes0, cvfull0, cvempty0)) {
+            aborted = true;
+            break;
         }
     }
     // After a give-up, wait (bounded) for this warp's copies still in flight, so that
@@ -488,6 +510,197 @@ __global__ void B3G_LEAF_BOUNDS(C + 32)
             mbar_wait_bounded(fullw + 8 * st, (i / S) & 1u, a.wait_limit_ns);
         }
     }
+}
+
+// ---------------------------------------------------------------------------------
+// Asynchronous-copy kernel: the same tiles, reducer warp and node buffers as the
+// bulk-tensor-copy kernel; only the staging differs.  Every lane of a consumer warp
+// copies 16-byte units of the warp's own 32 chunk rows with cp.async: copy i of lane l
+// brings unit l >> 3 (of the four of a 64-byte block) of row (l & 7) + 8 i, so that
+// one copy instruction reads 8 rows x 64 contiguous bytes.  A stage is laid out
+// unit-major, [unit 0..3][row 0..31][16 bytes]: an instruction's copies land in four
+// runs of 128 contiguous bytes, and lane r's four 128-bit reads of its row are 512
+// bytes apart, so neither side has bank conflicts and no swizzle is needed.  Each lane
+// waits for its own copy groups (cp.async.wait_group, a hardware wait for the thread's
+// own copies) and a warp barrier makes the other lanes' copies visible; all lanes
+// refill a stage right after the warp has read it.  No elected lane, no mbarrier and
+// no tensor map on the data path.
+//   S  stages in each consumer warp's ring, 2 KiB each (one 64-byte block of 32 rows)
+// ---------------------------------------------------------------------------------
+template <int C, int S, bool MIS>
+struct AsyncCfg {
+    // a stage holds 4 16-byte units of each of the 32 rows, 5 for a misaligned input
+    static constexpr uint32_t kUnits = MIS ? 5 : 4;
+    using Base = TmaCfg<C, S, 64, false, kUnits * 512>;
+    // rings, node buffers and reducer buffers as in the bulk-tensor-copy kernel, then
+    // the 4 node-buffer barriers, aligned to 128 bytes
+    static constexpr size_t kSmemBytes = 128 + size_t(Base::kOffBars) + 8 * 4;
+};
+
+// Resident CTAs per SM asked of the register allocator for the asynchronous-copy
+// kernel: 5 for 128-chunk tiles (at most 80 registers; the consumers need 56, the
+// reducer's tree code drives the count), none otherwise.
+#ifndef B3G_ASYNC_MIN_BLOCKS
+#define B3G_ASYNC_MIN_BLOCKS 5
+#endif
+
+// Words m[0..15] of a block that starts `sh` / 8 + 4 Q bytes into the 20 words x: each
+// funnel-shifted out of two neighbours (sh = 0 takes the word as it is).
+template <int Q>
+__device__ __forceinline__ void shifted_words(const uint32_t x[20], uint32_t sh, uint32_t m[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = __funnelshift_r(x[i + Q], x[i + Q + 1], sh);
+}
+
+template <int C, int S, bool CHUNK_CVS, uint32_t MODE, bool MIS>
+__global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) leaf_async_kernel(const LeafArgs a) {
+    using Cfg = TmaCfg<C, S, 64, CHUNK_CVS, AsyncCfg<C, S, MIS>::kUnits * 512>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t rings0 = (smem_u32(smem_raw) + 127u) & ~127u;
+    const uint32_t nodes0 = rings0 + Cfg::kOffNodes;  // buffer b at nodes0 + b * kNodeBytes
+    const uint32_t cvfull0 = rings0 + Cfg::kOffBars;  // 2: node buffer b is filled
+    const uint32_t cvempty0 = cvfull0 + 16;           // 2: node buffer b is free
+
+    const uint32_t tid = threadIdx.x;
+    const uint32_t warp = tid >> 5;
+    const uint32_t lane = tid & 31u;
+
+    grid_dependency_wait();  // see leaf_tma_kernel
+    if (tid == 0) {
+        launch_dependents();
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(cvfull0 + 8 * b, C);
+            mbar_init(cvempty0 + 8 * b, 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    uint32_t key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) key[i] = a.key[i];
+
+    if (warp == Cfg::kReducerWarp) {
+        if constexpr (!CHUNK_CVS) reducer_warp<Cfg, MODE>(a, key, rings0, nodes0, cvfull0, cvempty0);
+        return;
+    }
+
+    // --------------------------------- consumers ---------------------------------
+    const uint32_t ring = rings0 + warp * Cfg::kRingBytes;
+    const uint32_t rd = ring + lane * 16u;                             // unit u of row `lane`: + 512 u
+    const uint32_t wr = ring + (lane >> 3) * 512u + (lane & 7u) * 16u;  // copy i: + 128 i
+    const uint32_t lrow = warp * 32u + (lane & 7u);                     // copy i: row lrow + 8 i of a tile
+    // A misaligned input (MIS) is read as the 16-byte units of the aligned-down range:
+    // its block b of row r lies in units 4 b .. 4 b + 4 counted from `base` + 1024 r,
+    // starting `skew` bytes into the first.  Units 0..3 are copied as for an aligned
+    // input; the fifth by a fifth copy per lane, of the lane's own row.  Every unit copied
+    // holds at least one byte of the input, so none crosses a page the input does not
+    // touch.
+    const uint32_t skew = MIS ? static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a.in) & 15u) : 0u;
+    const uint8_t *base = a.in - skew;
+
+    // Fetch stream of this warp: fetch f brings block f mod 16 of the CTA's (f / 16)-th
+    // tile into stage f mod S; `fp` is the lane's source of the next fetch (its unit of
+    // row lrow of that tile, at that block).  The first `nfull` fetches are of tiles
+    // whose 32 rows (of this warp) are all full chunks.  Only the last tile of the input
+    // can hold other rows, and past the CTA's last tile come S fetches of no tile; those
+    // fetches copy the full-chunk rows alone, found from the row of `fp`: the other rows'
+    // CVs are discarded, or recomputed from global memory for the partial chunk.  Every
+    // fetch closes one copy group.
+    const uint64_t my_tiles = (a.n_tiles - 1 - blockIdx.x) / gridDim.x + 1;  // grid <= tiles
+    const uint64_t last_tile = blockIdx.x + (my_tiles - 1) * gridDim.x;
+    const uint32_t nfull = static_cast<uint32_t>(
+        16 * (last_tile * C + warp * 32u + 32u <= a.n_full ? my_tiles : my_tiles - 1));
+    const uint64_t jump = static_cast<uint64_t>(gridDim.x) * C * kChunkBytes - 15u * 64u;
+    const uint8_t *fp = base + (static_cast<uint64_t>(blockIdx.x) * C + lrow) * kChunkBytes + (lane >> 3) * 16u;
+    // the fifth unit of the lane's own row (MIS): row warp * 32 + lane, unit 4
+    const uint32_t fifth_off = (warp * 32u + lane) * static_cast<uint32_t>(kChunkBytes) + 64u -
+                               (lrow * static_cast<uint32_t>(kChunkBytes) + (lane >> 3) * 16u);
+    const uint32_t d5 = ring + 4u * 512u + lane * 16u;
+    uint32_t f = 0;
+    auto fetch = [&](uint32_t st) {
+        const uint32_t d = wr + st * Cfg::kStageBytes;
+        if (f < nfull) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cp_async16(d + 128u * i, fp + 8192u * i);
+            if constexpr (MIS) cp_async16(d5 + st * Cfg::kStageBytes, fp + fifth_off);
+        } else {
+            const uint64_t row = static_cast<uint64_t>(fp - base) / kChunkBytes;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (row + 8u * i < a.n_full) cp_async16(d + 128u * i, fp + 8192u * i);
+            if constexpr (MIS) {
+                if (row - (lane & 7u) + lane < a.n_full) cp_async16(d5 + st * Cfg::kStageBytes, fp + fifth_off);
+            }
+        }
+        cp_async_commit();
+        fp += (f & 15u) == 15u ? jump : 64u;
+        ++f;
+    };
+#pragma unroll
+    for (int j = 0; j < S; ++j) fetch(static_cast<uint32_t>(j));
+
+    uint32_t st = 0;  // stage of the next block
+    uint32_t k = 0;
+    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
+        const uint64_t chunk = tile * C + tid;
+        const uint64_t ctr = a.counter_base + chunk;
+        const uint32_t ctr_lo = static_cast<uint32_t>(ctr);
+        const uint32_t ctr_hi = static_cast<uint32_t>(ctr >> 32);
+        const uint32_t end_flags = kChunkEnd | ((a.root && a.n_chunks == 1) ? kRoot : 0u);
+
+        // Every thread compresses its row as a full chunk; the owner of the partial
+        // last chunk redoes its chunk in finish_tile.
+        uint32_t cv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cv[i] = key[i];
+        uint32_t flags = MODE | kChunkStart;
+
+#pragma unroll 1
+        for (uint32_t b = 0; b < 16; ++b) {
+            cp_async_wait<S - 1>();  // this lane's copies of block b have landed
+            __syncwarp();            // ... and every other lane's
+            const uint32_t rs = rd + st * Cfg::kStageBytes;
+            uint32_t m[16];
+            if constexpr (MIS) {
+                uint32_t x[20];
+#pragma unroll
+                for (int q = 0; q < 5; ++q) {
+                    const uint4 w = lds128(rs + 512u * q);
+                    x[4 * q + 0] = w.x;
+                    x[4 * q + 1] = w.y;
+                    x[4 * q + 2] = w.z;
+                    x[4 * q + 3] = w.w;
+                }
+                const uint32_t sh = (skew & 3u) * 8u;
+                switch (skew >> 2) {  // the same for every lane and block
+                    case 0: shifted_words<0>(x, sh, m); break;
+                    case 1: shifted_words<1>(x, sh, m); break;
+                    case 2: shifted_words<2>(x, sh, m); break;
+                    default: shifted_words<3>(x, sh, m); break;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w = lds128(rs + 512u * q);
+                    m[4 * q + 0] = w.x;
+                    m[4 * q + 1] = w.y;
+                    m[4 * q + 2] = w.z;
+                    m[4 * q + 3] = w.w;
+                }
+            }
+            compress(cv, m, ctr_lo, ctr_hi, 64u, b == 15 ? (flags | end_flags) : flags);
+            flags = MODE;
+            __syncwarp();  // every lane has read stage st: refill it, S blocks ahead
+            fetch(st);
+            if (++st == S) st = 0;
+        }
+        // the decision to leave is the warp's, so that no lane misses a warp barrier
+        const bool ok = finish_tile<Cfg, CHUNK_CVS, MODE>(a, key, cv, chunk, ctr, end_flags, k, nodes0, cvfull0,
+                                                          cvempty0);
+        if (__any_sync(0xffffffffu, !ok)) break;
+    }
+    cp_async_wait<0>();  // no copy may land after the CTA has left
 }
 
 // ---------------------------------------------------------------------------------
@@ -606,6 +819,20 @@ struct Tuning<32> {
     static constexpr int S = 4, LOAD = 128;
 };
 
+// Staging of the leaf kernel for 16-byte aligned inputs: 1 = per-lane asynchronous
+// copies (leaf_async_kernel), 0 = bulk tensor copies (leaf_tma_kernel); and the stage
+// count of the asynchronous-copy rings per tile size.
+#ifndef B3G_STAGING
+#define B3G_STAGING 0
+#endif
+#ifndef B3G_ASYNC_S
+#define B3G_ASYNC_S 2
+#endif
+template <int C>
+struct AsyncTuning {
+    static constexpr int S = B3G_ASYNC_S;
+};
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -697,6 +924,36 @@ b3g_status launch_tma(const LeafArgs &a, cudaStream_t stream, int dev, const Dev
     return e == cudaSuccess ? B3G_OK : cuda_fail(e, "leaf_tma_kernel launch");
 }
 
+template <int C, bool CV, uint32_t MODE, bool MIS>
+b3g_status launch_async(const LeafArgs &a, cudaStream_t stream, int dev, const DeviceInfo &info) {
+    constexpr int S = AsyncTuning<C>::S;
+    constexpr size_t smem = AsyncCfg<C, S, MIS>::kSmemBytes;
+    auto kernel = leaf_async_kernel<C, S, CV, MODE, MIS>;
+    int bps = 0;
+    b3g_status st = kernel_blocks_per_sm(reinterpret_cast<const void *>(kernel), C + 32, smem, dev, bps);
+    if (st != B3G_OK) return st;
+    const uint64_t grid = grid_for(a.n_tiles, bps, info.sm_count);
+    cudaError_t e = launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(C + 32), smem, stream, a);
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "leaf_async_kernel launch");
+}
+
+// Which leaf kernel takes an input: a staged kernel for inputs with at least one full
+// chunk (the bulk-tensor-copy kernel needs a 16-byte aligned base; the asynchronous-copy
+// kernel takes any base, shifting misaligned blocks out of the aligned-down units), the
+// plain-load kernel for the rest.
+enum class LeafPath { kDirect, kStaged, kStagedMisaligned };
+
+template <int C, bool CV, uint32_t MODE>
+b3g_status launch_staged(const LeafArgs &a, LeafPath path, cudaStream_t stream, int dev, const DeviceInfo &info) {
+#if B3G_STAGING
+    return path == LeafPath::kStagedMisaligned ? launch_async<C, CV, MODE, true>(a, stream, dev, info)
+                                               : launch_async<C, CV, MODE, false>(a, stream, dev, info);
+#else
+    (void)path;
+    return launch_tma<C, CV, MODE>(a, stream, dev, info);
+#endif
+}
+
 template <int C, bool CV, uint32_t MODE>
 b3g_status launch_direct(const LeafArgs &a, cudaStream_t stream, int dev, const DeviceInfo &info) {
     auto kernel = leaf_direct_kernel<C, CV, MODE>;
@@ -711,17 +968,18 @@ b3g_status launch_direct(const LeafArgs &a, cudaStream_t stream, int dev, const 
 // The hash mode is a template parameter of the kernels, so that the keyed kernels
 // compile exactly as without a mode; chunk CVs exist in keyed mode only.
 template <int C>
-b3g_status launch_c(const LeafArgs &a, bool chunk_cvs, bool tma, cudaStream_t stream, int dev,
+b3g_status launch_c(const LeafArgs &a, bool chunk_cvs, LeafPath path, cudaStream_t stream, int dev,
                     const DeviceInfo &info) {
+    const bool staged = path != LeafPath::kDirect;
     if (a.mode_flags == kModeDefault) {
         if (chunk_cvs) return B3G_ERR_ARG;
-        return tma ? launch_tma<C, false, kModeDefault>(a, stream, dev, info)
-                   : launch_direct<C, false, kModeDefault>(a, stream, dev, info);
+        return staged ? launch_staged<C, false, kModeDefault>(a, path, stream, dev, info)
+                      : launch_direct<C, false, kModeDefault>(a, stream, dev, info);
     }
     if (a.mode_flags != kModeKeyed) return B3G_ERR_ARG;
-    if (tma)
-        return chunk_cvs ? launch_tma<C, true, kModeKeyed>(a, stream, dev, info)
-                         : launch_tma<C, false, kModeKeyed>(a, stream, dev, info);
+    if (staged)
+        return chunk_cvs ? launch_staged<C, true, kModeKeyed>(a, path, stream, dev, info)
+                         : launch_staged<C, false, kModeKeyed>(a, path, stream, dev, info);
     return chunk_cvs ? launch_direct<C, true, kModeKeyed>(a, stream, dev, info)
                      : launch_direct<C, false, kModeKeyed>(a, stream, dev, info);
 }
@@ -732,12 +990,20 @@ const char *kernel_config() {
     static char buf[160];
     static std::once_flag once;
     std::call_once(once, [] {
+#if B3G_STAGING
+        std::snprintf(buf, sizeof buf,
+                      "leaf_async_kernel<%d,%d> min_blocks=%d g_form=%d top_batch=%d pair_noinline=%d "
+                      "rot_fma=0x%x pdl=1 modes=2",
+                      1 << kDefaultLeavesLog2, AsyncTuning<(1 << kDefaultLeavesLog2)>::S, B3G_MIN_BLOCKS,
+                      B3G_G_FORM, B3G_TOP_BATCH, B3G_PAIR_NOINLINE, static_cast<unsigned>(B3G_ROT_FMA));
+#else
         std::snprintf(buf, sizeof buf,
                       "leaf_tma_kernel<%d,%d,%d> unroll=%d min_blocks=%d g_form=%d top_batch=%d pair_noinline=%d "
                       "rot_fma=0x%x pdl=1 modes=2",
                       1 << kDefaultLeavesLog2, Tuning<(1 << kDefaultLeavesLog2)>::S,
                       Tuning<(1 << kDefaultLeavesLog2)>::LOAD, kCopyLoopUnroll, B3G_MIN_BLOCKS, B3G_G_FORM,
                       B3G_TOP_BATCH, B3G_PAIR_NOINLINE, static_cast<unsigned>(B3G_ROT_FMA));
+#endif
     });
     return buf;
 }
@@ -749,15 +1015,19 @@ b3g_status launch_leaf(const LeafArgs &a, int leaves_log2, bool chunk_cvs, cudaS
     DeviceInfo info;
     b3g_status st = device_info(dev, info);
     if (st != B3G_OK) return st;
-    // The tensor map needs a 16-byte aligned base, at least one full chunk, and
-    // row coordinates that fit in int32.
-    const bool tma = a.n_full >= 1 && (reinterpret_cast<uintptr_t>(a.in) & 15u) == 0 &&
-                     a.n_full + 256 < (1ull << 31);
+    // Staged kernels need at least one full chunk (and, for the tensor map, row
+    // coordinates that fit in int32); the bulk-tensor-copy kernel also a 16-byte aligned
+    // base.
+    const bool full = a.n_full >= 1 && a.n_full + 256 < (1ull << 31);
+    const bool aligned = (reinterpret_cast<uintptr_t>(a.in) & 15u) == 0;
+    const LeafPath path = !full ? LeafPath::kDirect
+                          : aligned ? LeafPath::kStaged
+                                    : (B3G_STAGING ? LeafPath::kStagedMisaligned : LeafPath::kDirect);
     switch (leaves_log2) {
-        case 5: return launch_c<32>(a, chunk_cvs, tma, stream, dev, info);
-        case 6: return launch_c<64>(a, chunk_cvs, tma, stream, dev, info);
-        case 7: return launch_c<128>(a, chunk_cvs, tma, stream, dev, info);
-        case 8: return launch_c<256>(a, chunk_cvs, tma, stream, dev, info);
+        case 5: return launch_c<32>(a, chunk_cvs, path, stream, dev, info);
+        case 6: return launch_c<64>(a, chunk_cvs, path, stream, dev, info);
+        case 7: return launch_c<128>(a, chunk_cvs, path, stream, dev, info);
+        case 8: return launch_c<256>(a, chunk_cvs, path, stream, dev, info);
         default: return B3G_ERR_ARG;
     }
 }

@@ -27,8 +27,11 @@ namespace {
 // 65,536 CTA roots (16 GiB of input at 256 chunks per CTA) plus the 64 CVs of the
 // next reduction level, rounded up.
 constexpr size_t kNoAllocScratchBytes = (2u << 20) + 4096;
-// 256 chunks per CTA subtree: the scratch size above is computed for it.
+// Inputs above 2^16 chunks (64 MiB) use 256 chunks per CTA subtree: the scratch size
+// above is computed for it.  Smaller inputs use the one-shot digest's subtree size
+// (down to 32 chunks, so that every SM gets a CTA), at most 2048 roots.
 constexpr int kNoAllocLeavesLog2 = 8;
+constexpr uint64_t kNoAllocSmallChunks = 1ull << 16;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -70,8 +73,8 @@ extern "C" b3g_status blake3_keyed_hash_noalloc(const void *d_in, uint64_t len, 
     if (len > B3G_NOALLOC_MAX_LEN) return B3G_ERR_WORKSPACE;
 
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int t = kNoAllocLeavesLog2;
     const uint64_t n_chunks = len == 0 ? 1 : ceil_div(len, kChunkBytes);
+    const int t = n_chunks <= kNoAllocSmallChunks ? leaves_log2_for(n_chunks) : kNoAllocLeavesLog2;
     const uint64_t tiles = ceil_div(n_chunks, 1ull << t);
     const uint64_t group = 1ull << kDefaultGroupLog2;
 

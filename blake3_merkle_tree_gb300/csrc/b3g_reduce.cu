@@ -80,6 +80,16 @@ __global__ void wait_probe_kernel(uint64_t limit_ns, int *flag) {
     *flag = done ? 0 : 1;
 }
 
+// The same probe reporting in a caller's status word: B3G_DEVICE_STATUS_TIMEOUT is ORed
+// into *status when the wait gives up, in stream order, as the hashing kernels do.
+__global__ void wait_probe_status_kernel(uint64_t limit_ns, uint32_t *status) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    if (!mbar_wait_bounded(b, 0, limit_ns)) atomicOr(status, B3G_DEVICE_STATUS_TIMEOUT);
+}
+
 // Compression-only loop: every thread runs `iters` chained compressions of the hashing
 // kernels' compress() with its message held in registers (fed back from the CV so that
 // nothing is hoisted) and no memory traffic; the ceiling the leaf kernel is measured
@@ -98,6 +108,108 @@ __global__ void __launch_bounds__(128) compress_rate_kernel(uint32_t seed, uint3
         m[5] ^= cv[3];
     }
     if ((cv[0] ^ cv[7]) == 0x5EED5EEDu && cv[1] == seed) *sink = cv[2];
+}
+
+// ---------------------------------------------------------------------------------
+// Several lanes per chunk (page section "未来工作": several threads could hash the same
+// chunk).  One compression spread over the 4 lanes of an aligned group of 4: lane q
+// holds column q of the state, v[q], v[4 + q], v[8 + q], v[12 + q].  The column step is
+// one G per lane; for the diagonal step rows 1, 2 and 3 are rotated by 1, 2 and 3 lanes
+// with shuffles, each lane runs one G, and the rows are rotated back.  w[r] holds the
+// lane's message words of round r (column x, y, diagonal x, y).  The output CV words q
+// and 4 + q stay on lane q, where the next compression of a chain takes them.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ void compress_4lane(uint32_t &cva, uint32_t &cvb, const uint32_t w[7][4], uint32_t q,
+                                               uint32_t counter_lo, uint32_t counter_hi, uint32_t block_len,
+                                               uint32_t flags) {
+    uint32_t a = cva, b = cvb;
+    uint32_t c = q == 0 ? kIv0 : q == 1 ? kIv1 : q == 2 ? kIv2 : kIv3;
+    uint32_t d = q == 0 ? counter_lo : q == 1 ? counter_hi : q == 2 ? block_len : flags;
+    const uint32_t up1 = (q + 1) & 3u, up2 = (q + 2) & 3u, up3 = (q + 3) & 3u;
+#pragma unroll
+    for (int r = 0; r < 7; ++r) {
+        g<0>(a, b, c, d, w[r][0], w[r][1]);
+        b = __shfl_sync(0xffffffffu, b, up1, 4);
+        c = __shfl_sync(0xffffffffu, c, up2, 4);
+        d = __shfl_sync(0xffffffffu, d, up3, 4);
+        g<4>(a, b, c, d, w[r][2], w[r][3]);
+        b = __shfl_sync(0xffffffffu, b, up3, 4);
+        c = __shfl_sync(0xffffffffu, c, up2, 4);
+        d = __shfl_sync(0xffffffffu, d, up1, 4);
+    }
+    cva = a ^ c;
+    cvb = b ^ d;
+}
+
+// The message words lane Q of a group of 4 needs in each round.
+template <int Q>
+__device__ __forceinline__ void lane_words(const uint32_t m[16], uint32_t w[7][4]) {
+#pragma unroll
+    for (int r = 0; r < 7; ++r) {
+        w[r][0] = m[msg_index(r, 2 * Q)];
+        w[r][1] = m[msg_index(r, 2 * Q + 1)];
+        w[r][2] = m[msg_index(r, 8 + 2 * Q)];
+        w[r][3] = m[msg_index(r, 9 + 2 * Q)];
+    }
+}
+
+// Latency of a chain of `chain` dependent keyed compressions in one warp: L = 1, one
+// chain per lane (32 chains, the hashing kernels' compress); L = 4, one chain per group
+// of 4 lanes (8 chains, compress_4lane).  Chain g starts from the key, compresses the
+// message m[i] = (16 g + i) * 0x9E3779B9 (mod 2^32) at counter j in step j, with block
+// length 64 and flags KEYED_HASH, and writes its final CV to out + 32 g.  Lane 0 writes
+// the clock cycles of the whole chain to *cycles.
+template <int L>
+__global__ void __launch_bounds__(32) compress_latency_kernel(uint32_t chain, const LatencyArgs a) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t gid = lane / L;
+    uint32_t m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = (16u * gid + static_cast<uint32_t>(i)) * 0x9E3779B9u;
+    long long t0, t1;
+    if constexpr (L == 1) {
+        uint32_t cv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cv[i] = a.key[i];
+        __syncwarp();
+        t0 = clock64();
+#pragma unroll 1
+        for (uint32_t j = 0; j < chain; ++j) compress(cv, m, j, 0u, kBlockLen, kModeKeyed);
+        t1 = clock64();
+        uint4 *o = reinterpret_cast<uint4 *>(a.out + 32ull * gid);
+        o[0] = make_uint4(cv[0], cv[1], cv[2], cv[3]);
+        o[1] = make_uint4(cv[4], cv[5], cv[6], cv[7]);
+    } else {
+        const uint32_t q = lane & 3u;
+        uint32_t w[7][4];
+        switch (q) {
+            case 0: lane_words<0>(m, w); break;
+            case 1: lane_words<1>(m, w); break;
+            case 2: lane_words<2>(m, w); break;
+            default: lane_words<3>(m, w); break;
+        }
+        uint32_t cva = a.key[q], cvb = a.key[4 + q];
+        __syncwarp();
+        t0 = clock64();
+#pragma unroll 1
+        for (uint32_t j = 0; j < chain; ++j) compress_4lane(cva, cvb, w, q, j, 0u, kBlockLen, kModeKeyed);
+        t1 = clock64();
+        uint32_t *o = reinterpret_cast<uint32_t *>(a.out + 32ull * gid);
+        o[q] = cva;
+        o[4 + q] = cvb;
+    }
+    if (lane == 0) *a.cycles = static_cast<unsigned long long>(t1 - t0);
+}
+
+b3g_status launch_compress_latency(int lanes, uint32_t chain, const LatencyArgs &a, cudaStream_t stream) {
+    if (lanes == 1)
+        compress_latency_kernel<1><<<1, 32, 0, stream>>>(chain, a);
+    else if (lanes == 4)
+        compress_latency_kernel<4><<<1, 32, 0, stream>>>(chain, a);
+    else
+        return B3G_ERR_ARG;
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "compress_latency_kernel launch");
 }
 
 b3g_status launch_compress_rate(uint32_t blocks, uint32_t iters, uint32_t *d_sink, cudaStream_t stream) {
@@ -123,6 +235,12 @@ b3g_status launch_wait_probe(uint64_t limit_ns, int *d_flag, cudaStream_t stream
     wait_probe_kernel<<<1, 1, 0, stream>>>(limit_ns, d_flag);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? B3G_OK : cuda_fail(e, "wait_probe_kernel launch");
+}
+
+b3g_status launch_wait_probe_status(uint64_t limit_ns, uint32_t *d_status, cudaStream_t stream) {
+    wait_probe_status_kernel<<<1, 1, 0, stream>>>(limit_ns, d_status);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "wait_probe_status_kernel launch");
 }
 
 }  // namespace b3g

@@ -29,7 +29,8 @@
  *   - All calls that take a stream are asynchronous on it: no host synchronisation
  *     and no device-to-host copy.  Errors found on the host (arguments, launch)
  *     are returned; errors found on the device (a bounded wait that gave up) are
- *     recorded in the device status word, read by blake3_device_status().
+ *     recorded in the device status word, read by blake3_device_status(), or in a
+ *     caller's own status word (blake3_keyed_hash_ex).
  *   - len == 0 is valid (the empty input has one empty chunk); d_in may then be NULL.
  *   - d_in may have any alignment.  A 16-byte aligned d_in with at least one full
  *     chunk takes the bulk-tensor-copy (TMA) path; other inputs take a path with
@@ -133,6 +134,25 @@ b3g_status blake3_keyed_hash_ws(const void *d_in, uint64_t len, const uint8_t ke
                                 b3g_stream_t stream);
 
 /*
+ * blake3_keyed_hash_ex -- as blake3_keyed_hash_ws (d_ws != NULL) or blake3_keyed_hash
+ * (d_ws == NULL: temporary workspace from the stream-ordered allocator), with a
+ * per-call status word.  d_status is a 4-byte aligned DEVICE word owned by the caller:
+ * a kernel of this call whose bounded wait gives up ORs B3G_DEVICE_STATUS_TIMEOUT into
+ * it, in stream order, instead of into the per-device word; the library never clears
+ * it.  So the outcome of this one call is known from a 4-byte device-to-host copy on
+ * `stream` after it, without synchronising the device or touching other streams' calls
+ * (the caller zeroes the word before the call, or keeps ORing several calls into it).
+ * With the word clear the digest in d_out32 is valid; with the bit set it is not.
+ * Failure detection of the leaf and reduction kernels (SURVEY: failure detection);
+ * the page has no counterpart.
+ * Errors: as blake3_keyed_hash_ws, plus B3G_ERR_NULL (d_status NULL) and
+ * B3G_ERR_ALIGN (d_status not 4-byte aligned).
+ */
+b3g_status blake3_keyed_hash_ex(const void *d_in, uint64_t len, const uint8_t key[32],
+                                uint8_t *d_out32, void *d_ws, size_t ws_bytes,
+                                uint32_t *d_status, b3g_stream_t stream);
+
+/*
  * blake3_hash / blake3_hash_ws -- the digest in the default (unkeyed) mode.  Page
  * section "BLAKE3": a chunk's first block starts from an IV by default and from the
  * user's key in keyed mode.  Here every chunk and every parent starts from the IV and
@@ -222,6 +242,34 @@ b3g_status blake3_device_status(uint32_t *status_out);
  * word.  Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_CUDA.
  */
 b3g_status blake3_selftest_bounded_wait(uint32_t limit_us, int *timed_out_out);
+
+/*
+ * blake3_selftest_bounded_wait_ex -- the same probe, asynchronous on `stream`,
+ * reporting like the hashing kernels of blake3_keyed_hash_ex: if its wait gives up
+ * (the expected outcome) it ORs B3G_DEVICE_STATUS_TIMEOUT into the caller's 4-byte
+ * aligned device word d_status, in stream order.  Errors: B3G_ERR_NULL, B3G_ERR_ARG
+ * (limit_us outside 1..10^7), B3G_ERR_ALIGN, B3G_ERR_CUDA.
+ */
+b3g_status blake3_selftest_bounded_wait_ex(uint32_t limit_us, uint32_t *d_status, b3g_stream_t stream);
+
+/*
+ * blake3_selftest_compress_latency -- several threads per chunk (page section
+ * "未来工作": threads could share the work of one chunk).  Launches ONE warp on `stream`
+ * that runs chains of `chain` (1..2^20) dependent keyed compressions:
+ *   lanes_per_chunk = 1: 32 chains, one per lane, with the hashing kernels' compression;
+ *   lanes_per_chunk = 4: 8 chains, one per group of 4 lanes, each lane holding one
+ *     column of the state (the column step is one G per lane; shuffles rotate the rows
+ *     for the diagonal step and back).
+ * Chain g starts from the key and compresses, in step j, the 64-byte block of words
+ * m[i] = (16 g + i) * 0x9E3779B9 (mod 2^32), i = 0..15, little-endian, with counter j,
+ * block length 64 and flags KEYED_HASH.  Chain g's final CV goes to d_cvs + 32 g
+ * (32 / lanes_per_chunk CVs, 16-byte aligned) and the clock cycles of lane 0's whole
+ * chain to *d_cycles (8-byte aligned): the dependency-chain latency of one compression
+ * is *d_cycles / chain.  Asynchronous.
+ * Errors: B3G_ERR_NULL, B3G_ERR_ARG, B3G_ERR_ALIGN, B3G_ERR_CUDA.
+ */
+b3g_status blake3_selftest_compress_latency(int lanes_per_chunk, uint32_t chain, const uint8_t key[32],
+                                            uint8_t *d_cvs, uint64_t *d_cycles, b3g_stream_t stream);
 
 /*
  * blake3_selftest_compress_rate -- launches `blocks` CTAs of 128 threads (1..2^20) on

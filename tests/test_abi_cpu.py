@@ -110,6 +110,13 @@ def test_argument_errors_before_any_cuda_call(lib):
     assert lib.blake3_device_status(None) == 1
     assert lib.blake3_selftest_bounded_wait(0, ctypes.byref(ctypes.c_int())) == 6
     assert lib.blake3_selftest_bounded_wait(10, None) == 1
+    ex = lib.blake3_keyed_hash_ex
+    assert ex(FAKE, 10, KEY, FAKE, None, 0, None, None) == 1  # no status word
+    assert ex(FAKE, 10, KEY, FAKE, None, 0, ctypes.c_void_p(0x10002), None) == 2  # status not 4-byte aligned
+    assert ex(FAKE, 1 << 30, KEY, FAKE, FAKE, 16, FAKE, None) == 3  # workspace too small
+    assert lib.blake3_selftest_bounded_wait_ex(10, None, None) == 1
+    assert lib.blake3_selftest_bounded_wait_ex(0, FAKE, None) == 6
+    assert lib.blake3_selftest_bounded_wait_ex(10, ctypes.c_void_p(0x10001), None) == 2
 
 
 def test_binding_refuses_host_tensors(lib):
@@ -176,7 +183,7 @@ def test_options_and_config(lib):
     assert lib.blake3_set_option(2, 0) == 0
     assert lib.blake3_set_option(3, 1) == 0 and lib.blake3_set_option(3, 0) == 0
     assert lib.blake3_set_option(1, 0) == 0
-    assert lib.blake3_kernel_config().startswith(b"leaf_tma_kernel<")
+    assert lib.blake3_kernel_config().startswith((b"leaf_async_kernel<", b"leaf_tma_kernel<"))
 
 
 def _state_record(magic=0x48473342, version=1, mode=16, depth=1, count=3000, pushed=2, acc_len=952,

@@ -3,8 +3,11 @@ at hashing time (their GPU memory is owned by another allocator, they cannot acc
 synchronisation an allocation may cause, or their policy forbids allocating after
 start-up).  It keeps its CTA roots in a fixed scratch array inside the library.
 
-Checked through the C ABI against blake3_keyed_hash, on two calls in a row with
-different inputs (the second call reuses the scratch the first one left behind).
+Checked through the C ABI against the CPU oracle and against blake3_keyed_hash, call
+after call (each call reuses the scratch the one before left behind), over every path
+the entry point can take: the empty input, inputs shorter than a chunk and than a CTA
+subtree (no scratch used), the small-input subtree sizes, a misaligned view (the
+plain-load kernel), and an input of more than 1024 CTA subtrees (two reduction levels).
 This file is collected last on purpose."""
 
 import ctypes
@@ -12,6 +15,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from blake3_merkle_tree_gb300 import binding, build, workloads
 
 pytestmark = pytest.mark.gpu
@@ -27,19 +31,25 @@ def _noalloc(lib, dev, key):
     return bytes(out.cpu().numpy())
 
 
-def test_noalloc_matches_blake3_keyed_hash_twice():
+# (length, byte offset of the view): 0, 1 and 1023 bytes fit one CTA subtree; 5 MiB + 3
+# takes the small-input subtree size; 9 MiB + 5 at offset 3 is misaligned; 300 MiB + 777
+# is 1201 subtrees of 256 chunks (two reduction levels)
+CASES = [(0, 0), (1, 0), (1023, 0), (5 * (1 << 20) + 3, 0), (9 * (1 << 20) + 5, 3), (300 * (1 << 20) + 777, 0)]
+
+
+def test_noalloc_matches_the_oracle_call_after_call():
     build.build()
     lib = binding.library()
     key = workloads.key_bytes(7)
-    # several tiles and a ragged tail, then a larger input with two reduction levels
-    sizes = [5 * (1 << 20) + 3, 300 * (1 << 20) + 777]
-    for n in sizes:
-        dev = workloads.uniform_bytes(n % 1000, n, device="cuda")
-        want = bytes(binding.blake3_keyed_hash(dev, key).cpu().numpy())
-        assert _noalloc(lib, dev, key) == want, n
-    # a single-tile input does not touch the scratch at all
-    small = workloads.uniform_bytes(3, 4000, device="cuda")
-    assert _noalloc(lib, small, key) == bytes(binding.blake3_keyed_hash(small, key).cpu().numpy())
+    for n, off in CASES:
+        host = workloads.uniform_bytes(n % 1000, n)
+        buf = torch.empty(n + off, dtype=torch.uint8, device="cuda")
+        buf[off:].copy_(host)
+        dev = buf[off:]
+        want = oracle.keyed_hash(host, key)
+        assert _noalloc(lib, dev, key) == want, (n, off)
+        assert bytes(binding.blake3_keyed_hash(dev, key).cpu().numpy()) == want, (n, off)
+        assert _noalloc(lib, dev, key) == want, (n, off)  # again, on the scratch the call above left
     assert binding.blake3_device_status() == 0
 
 
