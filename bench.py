@@ -42,6 +42,7 @@ WORKLOAD = "12GiB+777"
 OPS_PER_COMPRESSION = 7 * 8 * 12 + 8
 # The page's count ("7 rounds x 8 G x 6 operations = 336 per 64-byte block").
 PAGE_OPS_PER_COMPRESSION = 336
+DYNAMIC_MIN_TILES = 760  # above this many CTA subtrees the leaf kernel takes tiles from a counter
 INT32_LANES_PER_SM = 128  # integer instructions issued per SM per clock (4 schedulers x 32 lanes)
 
 
@@ -313,11 +314,19 @@ def _step_fn(lib, binding, dev, n, key, stream):
     roots = torch.empty((tiles, 32), dtype=torch.uint8, device="cuda")
     red_ws = torch.empty(max(16, lib.blake3_reduce_workspace_size(tiles, -1)), dtype=torch.uint8, device="cuda")
     out = torch.empty(32, dtype=torch.uint8, device="cuda")
+    counter = torch.zeros(4, dtype=torch.int32, device="cuda")  # the leaf kernel's tile counter
+
+    # as in the library's one-shot call: the counter only when there are more tiles than
+    # resident CTAs (below that every CTA has one tile)
+    dynamic = tiles > DYNAMIC_MIN_TILES
 
     def step(ev_a=None, ev_b=None):
+        if dynamic:
+            counter.zero_()
         if ev_a is not None:
             ev_a.record(stream)
-        st = lib.blake3_keyed_tile_roots(dev.data_ptr(), n, 0, key, leaves_log2, 1, roots.data_ptr(), sp)
+        st = lib.blake3_keyed_tile_roots_ex(dev.data_ptr(), n, 0, key, leaves_log2, 1, roots.data_ptr(),
+                                            counter.data_ptr() if dynamic else None, sp)
         if st:
             raise binding.B3GError(st, "blake3_keyed_tile_roots")
         if ev_b is not None:
@@ -358,16 +367,16 @@ def _measure_config(lib, binding, wname, steps, hbm_peak, int_peak, threads):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if small else None
     for _ in range(3):
         step()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for a, b, c in evs:
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(steps)]
+    for z, a, b, c in evs:
         if flush is not None:
             flush.fill_(1)
+        z.record(stream)
         step(a, b)
         c.record(stream)
     torch.cuda.synchronize()
-    step_ms = statistics.median(a.elapsed_time(c) for a, _, c in evs)
-    leaf_ms = statistics.median(a.elapsed_time(b) for a, b, _ in evs)
+    step_ms = statistics.median(z.elapsed_time(c) for z, _, _, c in evs)
+    leaf_ms = statistics.median(a.elapsed_time(b) for _, a, b, _ in evs)
     got = bytes(digest_t.cpu().numpy())
     t0 = time.perf_counter()
     ref = _oracle_digest_threaded(dev.cpu(), key, threads)
@@ -457,34 +466,15 @@ def run_ours(args):
     n = w.nbytes
     dev = w.data(device="cuda")
     stream = torch.cuda.current_stream()
-    sp = stream.cuda_stream
     leaves_log2 = lib.blake3_default_leaves_log2()
-    tiles = lib.blake3_tile_count(n, leaves_log2)
-    roots = torch.empty((tiles, 32), dtype=torch.uint8, device="cuda")
-    red_ws = torch.empty(max(16, lib.blake3_reduce_workspace_size(tiles, -1)), dtype=torch.uint8, device="cuda")
-    out = torch.empty(32, dtype=torch.uint8, device="cuda")
-    kp = key
-
-    def step(ev_a=None, ev_b=None):
-        if ev_a is not None:
-            ev_a.record(stream)
-        st = lib.blake3_keyed_tile_roots(dev.data_ptr(), n, 0, kp, leaves_log2, 1, roots.data_ptr(), sp)
-        if st:
-            raise binding.B3GError(st, "blake3_keyed_tile_roots")
-        if ev_b is not None:
-            ev_b.record(stream)
-        if tiles > 1:
-            st = lib.blake3_keyed_reduce_cvs(roots.data_ptr(), tiles, kp, 1, -1, out.data_ptr(), red_ws.data_ptr(),
-                                             red_ws.numel(), sp)
-            if st:
-                raise binding.B3GError(st, "blake3_keyed_reduce_cvs")
-
-    launches = 1 + _reduce_launches(tiles)  # per step: the leaf launch and the reduction levels
+    # per step: the tile counter zeroed, the leaf launch (timed alone as well), the
+    # reduction launches
+    step, digest_t, launches, tiles = _step_fn(lib, binding, dev, n, key, stream)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    digest_bench = bytes((roots[0] if tiles == 1 else out).cpu().numpy())
+    digest_bench = bytes(digest_t.cpu().numpy())
     digest_api = bytes(binding.blake3_keyed_hash(dev, key).cpu().numpy())
     if digest_bench != digest_api:
         raise RuntimeError("bench step and blake3_keyed_hash disagree")

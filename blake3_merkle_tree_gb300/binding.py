@@ -62,6 +62,7 @@ def library() -> ctypes.CDLL:
             "blake3_keyed_subtree_root": (i32, [vp, u64, u64, vp, i32, vp, vp]),
             "blake3_tile_count": (u64, [u64, i32]),
             "blake3_keyed_tile_roots": (i32, [vp, u64, u64, vp, i32, i32, vp, vp]),
+            "blake3_keyed_tile_roots_ex": (i32, [vp, u64, u64, vp, i32, i32, vp, vp, vp]),
             "blake3_reduce_workspace_size": (sz, [u64, i32]),
             "blake3_keyed_reduce_cvs": (i32, [vp, u64, vp, i32, i32, vp, vp, sz, vp]),
             "blake3_device_status": (i32, [ctypes.POINTER(ctypes.c_uint32)]),
@@ -239,8 +240,11 @@ def blake3_tile_count(nbytes: int, leaves_log2: int = -1) -> int:
 
 
 def blake3_keyed_tile_roots(data: torch.Tensor, key, chunk_offset: int = 0, leaves_log2: int = -1,
-                            is_root: bool = False, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """CTA subtree roots as a (tiles, 32) uint8 CUDA tensor."""
+                            is_root: bool = False, out: torch.Tensor | None = None, stream=None,
+                            tile_counter: torch.Tensor | None = None) -> torch.Tensor:
+    """CTA subtree roots as a (tiles, 32) uint8 CUDA tensor.  With `tile_counter` (a CUDA
+    word the caller has zeroed on the stream) the tiles are scheduled dynamically
+    (blake3_keyed_tile_roots_ex)."""
     tiles = blake3_tile_count(_nbytes(data), leaves_log2)
     if tiles == 0:
         raise B3GError(6, "blake3_keyed_tile_roots", "leaves_log2 out of range")
@@ -248,9 +252,10 @@ def blake3_keyed_tile_roots(data: torch.Tensor, key, chunk_offset: int = 0, leav
         out = torch.empty((tiles, 32), dtype=torch.uint8, device=data.device)
     if _nbytes(out) < 32 * tiles:
         raise ValueError("tile root output too small")
-    st = library().blake3_keyed_tile_roots(_dev_ptr(data, "data"), _nbytes(data), chunk_offset, _key(key),
-                                           leaves_log2, int(is_root), _dev_ptr(out, "out"), _stream(stream))
-    _check(st, "blake3_keyed_tile_roots")
+    st = library().blake3_keyed_tile_roots_ex(_dev_ptr(data, "data"), _nbytes(data), chunk_offset, _key(key),
+                                              leaves_log2, int(is_root), _dev_ptr(out, "out"),
+                                              _dev_ptr(tile_counter, "tile_counter"), _stream(stream))
+    _check(st, "blake3_keyed_tile_roots_ex")
     return out
 
 

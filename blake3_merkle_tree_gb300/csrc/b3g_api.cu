@@ -127,6 +127,7 @@ LeafArgs leaf_args(const void *d_in, uint64_t len, uint64_t chunk_offset, const 
     a.tail_bytes = static_cast<uint32_t>(len % kChunkBytes);
     a.ticket = nullptr;
     a.final_out = nullptr;
+    a.tile_counter = nullptr;
     return a;
 }
 
@@ -181,19 +182,28 @@ b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, con
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(ticket)");
         return launch_leaf(a, t, false, stream);
     }
+    const int g = reduce_group_log2(a.n_tiles);
+    if (a.n_tiles > kDynamicMinTiles && leaf_takes_tile_counter(d_in, a.n_full)) {
+        // the tile counter sits after the reduction levels
+        a.tile_counter = reinterpret_cast<uint32_t *>(ws + round16(a.n_tiles * 32) + reduce_ws(a.n_tiles, g));
+        cudaError_t e = cudaMemsetAsync(a.tile_counter, 0, sizeof(uint32_t), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(tile counter)");
+    }
     st = launch_leaf(a, t, false, stream);
     if (st != B3G_OK) return st;
-    return reduce_levels(ws, a.n_tiles, a.key, mode_flags, root, reduce_group_log2(a.n_tiles), d_out32,
-                         ws + round16(a.n_tiles * 32), stream);
+    return reduce_levels(ws, a.n_tiles, a.key, mode_flags, root, g, d_out32, ws + round16(a.n_tiles * 32),
+                         stream);
 }
 
 size_t hash_workspace(uint64_t len) {
     const uint64_t n = n_chunks_of(len);
     const uint64_t tiles = ceil_div(n, 1ull << choose_leaves_log2(n));
     if (tiles == 1) return 0;
-    // the fused path needs 16 bytes for its ticket counter instead of reduction levels
+    // the fused path needs 16 bytes for its ticket counter instead of reduction levels;
+    // inputs of more than kDynamicMinTiles tiles 16 bytes for a tile counter
     const size_t levels = reduce_ws(tiles, reduce_group_log2(tiles));
-    return round16(tiles * 32) + (tiles <= kMaxFusedTiles && levels < 16 ? 16 : levels);
+    return round16(tiles * 32) + (tiles <= kMaxFusedTiles && levels < 16 ? 16 : levels) +
+           (tiles > kDynamicMinTiles ? 16 : 0);
 }
 
 // Runs hash_range with a stream-ordered temporary workspace.
@@ -403,17 +413,24 @@ uint64_t blake3_tile_count(uint64_t len, int leaves_log2) {
     return ceil_div(n_chunks_of(len), 1ull << leaves_log2);
 }
 
-b3g_status blake3_keyed_tile_roots(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
-                                   int leaves_log2, int is_root, uint8_t *d_roots, b3g_stream_t stream) {
+b3g_status blake3_keyed_tile_roots_ex(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
+                                      int leaves_log2, int is_root, uint8_t *d_roots, uint32_t *d_tile_counter,
+                                      b3g_stream_t stream) {
     if (!key || !d_roots || (!d_in && len > 0)) return B3G_ERR_NULL;
-    if (misaligned16(d_roots)) return B3G_ERR_ALIGN;
+    if (misaligned16(d_roots) || (reinterpret_cast<uintptr_t>(d_tile_counter) & 3u)) return B3G_ERR_ALIGN;
     if (leaves_log2 == -1) leaves_log2 = kDefaultLeavesLog2;
     if (!valid_leaves_log2(leaves_log2)) return B3G_ERR_ARG;
     uint32_t *status = nullptr;
     b3g_status st = status_word(&status);
     if (st != B3G_OK) return st;
     LeafArgs a = leaf_args(d_in, len, chunk_offset, key, kModeKeyed, leaves_log2, is_root != 0, d_roots, status);
+    a.tile_counter = d_tile_counter;
     return launch_leaf(a, leaves_log2, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+b3g_status blake3_keyed_tile_roots(const void *d_in, uint64_t len, uint64_t chunk_offset, const uint8_t key[32],
+                                   int leaves_log2, int is_root, uint8_t *d_roots, b3g_stream_t stream) {
+    return blake3_keyed_tile_roots_ex(d_in, len, chunk_offset, key, leaves_log2, is_root, d_roots, nullptr, stream);
 }
 
 size_t blake3_reduce_workspace_size(uint64_t count, int group_log2) {

@@ -231,6 +231,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test with a suspend-time hint: a thread whose phase has not completed may be
+// suspended until it completes or about `hint_ns` nanoseconds have passed, instead of
+// returning at once to poll again.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Suspend-time hint of the bounded waits (0: none, the hardware's own limit).
+#ifndef B3G_WAIT_HINT_NS
+#define B3G_WAIT_HINT_NS 0
+#endif
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -244,7 +264,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
+#if B3G_WAIT_HINT_NS
+        if (mbar_try_wait_hint(bar, parity, B3G_WAIT_HINT_NS)) return true;
+#else
         if (mbar_try_wait(bar, parity)) return true;
+#endif
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
@@ -316,6 +340,16 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
     return v;
+}
+
+__device__ __forceinline__ uint64_t lds64(uint32_t addr) {
+    uint64_t v;
+    asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void sts64(uint32_t addr, uint64_t v) {
+    asm volatile("st.shared.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {

@@ -70,7 +70,18 @@ struct LeafArgs {
     // to the root, with ROOT when `root` is set, and writes it to `final_out`.
     uint32_t *ticket;
     uint8_t *final_out;
+    // Dynamic tile scheduling (asynchronous-copy kernel only): a zeroed counter from
+    // which the CTAs take their tiles after the first (NULL: tiles blockIdx.x + i gridDim.x).
+    uint32_t *tile_counter;
 };
+
+// Inputs with more tiles than this take their tiles from a counter (the CTA count of a
+// 128-chunk launch is 5 per SM, 760 on GB300: below it every CTA has one tile).
+constexpr uint64_t kDynamicMinTiles = 760;
+
+// Whether launch_leaf would run a kernel that takes tiles from LeafArgs::tile_counter
+// for an input at `in` with `n_full` full chunks.
+bool leaf_takes_tile_counter(const void *in, uint64_t n_full);
 
 // Largest tile count the fused final reduction handles (one CV per lane of a warp).
 constexpr uint64_t kMaxFusedTiles = 32;

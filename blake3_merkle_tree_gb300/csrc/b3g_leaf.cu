@@ -208,11 +208,25 @@ __device__ __forceinline__ void fused_final_reduce(const LeafArgs &a, const uint
     }
 }
 
+// Tile index ring of the asynchronous-copy kernel: at the start of its k-th tile
+// (counting from 0) the CTA publishes its (k + 1)-th tile in slot k mod kTileSlots, and
+// barrier k mod kTileSlots completes once per publication (parity (k / kTileSlots) & 1).
+// Four slots suffice: slot k mod 4 is rewritten at the start of tile k + 4, which the
+// publishing warp reaches only after the node buffer of tile k + 2 was handed over, so
+// after every consumer warp (which reads the slot during tile k) and the reducer (after
+// tile k) have read it.
+constexpr uint32_t kTileSlots = 4;
+
 // The reducer warp of the leaf kernels (page sections "Merkle Tree 归约" and "未来工作"):
-// turns each tile's chunk CVs, handed over in node buffer k & 1, into the tile CV.
+// turns each tile's chunk CVs, handed over in node buffer k & 1, into the tile CV.  The
+// CTA's tiles are blockIdx.x, blockIdx.x + gridDim.x, ... (`slots` == 0) or the ones
+// published in the tile index ring at `slots` (the first is blockIdx.x): the tile after
+// the k-th was published before the consumers' hand-over of the k-th, which the reducer
+// has waited for, so reading it needs no further wait.
 template <typename Cfg, uint32_t MODE>
 __device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t key[8], uint32_t rings0,
-                                             uint32_t nodes0, uint32_t cvfull0, uint32_t cvempty0) {
+                                             uint32_t nodes0, uint32_t cvfull0, uint32_t cvempty0,
+                                             uint32_t slots = 0) {
     constexpr int C = Cfg::kC;
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t scratch1 = rings0 + Cfg::kOffScratch1;
@@ -228,7 +242,7 @@ __device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t k
     // array (pairing never mixes two tiles: each holds a power-of-two count),
     // so those levels keep whole warps busy instead of 16, 8, 4, 2 and 1 lanes.
     uint32_t pending = 0;  // tiles waiting in top A
-    uint64_t first = 0;    // the first of them (the others follow at gridDim.x)
+    uint64_t my_tile = 0;  // lane p: the index of pending tile p
     auto flush = [&]() {
         if (pending == 0) return;
         uint32_t n = pending * 32u, src = topA, dst = topB;
@@ -243,7 +257,7 @@ __device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t k
         if (lane < pending) {
             uint32_t x[8];
             load_node(src, lane, x);
-            uint4 *o = reinterpret_cast<uint4 *>(a.out + (first + static_cast<uint64_t>(lane) * gridDim.x) * 32);
+            uint4 *o = reinterpret_cast<uint4 *>(a.out + my_tile * 32);
             o[0] = make_uint4(x[0], x[1], x[2], x[3]);
             o[1] = make_uint4(x[4], x[5], x[6], x[7]);
         }
@@ -251,7 +265,7 @@ __device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t k
         pending = 0;
     };
     uint32_t k = 0;
-    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
+    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; ++k) {
         const uint32_t b = k & 1u;
         const uint32_t src0 = nodes0 + b * Cfg::kNodeBytes;
         if (!mbar_wait_bounded(cvfull0 + 8 * b, (k >> 1) & 1u, a.wait_limit_ns)) {
@@ -279,8 +293,9 @@ __device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t k
                 store_node(slot, lane, x);
                 __syncwarp();
             }
-            if (pending == 0) first = tile;
+            if (lane == pending) my_tile = tile;
             if (++pending == Cfg::kTopBatch) flush();
+            tile = slots ? lds64(slots + 8 * (k % kTileSlots)) : tile + gridDim.x;
             continue;
         }
         // a partial tile, a single-tile root or the fused final reduction: on its own
@@ -316,8 +331,23 @@ __device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t k
             o[1] = make_uint4(x[4], x[5], x[6], x[7]);
         }
         if (a.ticket) fused_final_reduce(a, key, MODE);
+        tile = slots ? lds64(slots + 8 * (k % kTileSlots)) : tile + gridDim.x;
     }
     flush();
+}
+
+// The reducer warp as a called function, for the asynchronous-copy kernel: inlined
+// there, the tree code's registers and the consumers' fetch state compete in one
+// allocation and ptxas spills (52 bytes of reloads at five CTAs per SM); called, the
+// kernel keeps 72 registers and the aligned kernel spills nothing.
+template <typename Cfg, uint32_t MODE>
+__device__ __noinline__ void reducer_warp_call(const LeafArgs &a, const uint32_t *key, uint32_t rings0,
+                                               uint32_t nodes0, uint32_t cvfull0, uint32_t cvempty0,
+                                               uint32_t slots) {
+    uint32_t k8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) k8[i] = key[i];
+    reducer_warp<Cfg, MODE>(a, k8, rings0, nodes0, cvfull0, cvempty0, slots);
 }
 
 // End of a consumer thread's tile: the owner of the partial last chunk redoes it from
@@ -533,8 +563,9 @@ struct AsyncCfg {
     static constexpr uint32_t kUnits = MIS ? 5 : 4;
     using Base = TmaCfg<C, S, 64, false, kUnits * 512>;
     // rings, node buffers and reducer buffers as in the bulk-tensor-copy kernel, then
-    // the 4 node-buffer barriers, aligned to 128 bytes
-    static constexpr size_t kSmemBytes = 128 + size_t(Base::kOffBars) + 8 * 4;
+    // the 4 node-buffer barriers, the 4 tile-slot barriers and the 4 tile slots,
+    // aligned to 128 bytes
+    static constexpr size_t kSmemBytes = 128 + size_t(Base::kOffBars) + 96;
 };
 
 // Resident CTAs per SM asked of the register allocator for the asynchronous-copy
@@ -552,14 +583,23 @@ __device__ __forceinline__ void shifted_words(const uint32_t x[20], uint32_t sh,
     for (int i = 0; i < 16; ++i) m[i] = __funnelshift_r(x[i + Q], x[i + Q + 1], sh);
 }
 
+// Block of a tile at which thread 0 takes the CTA's next tile from the counter.
+#ifndef B3G_GRAB_BLOCK
+#define B3G_GRAB_BLOCK 14
+#endif
+constexpr uint32_t kGrabBlock = B3G_GRAB_BLOCK;
+
 template <int C, int S, bool CHUNK_CVS, uint32_t MODE, bool MIS>
 __global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) leaf_async_kernel(const LeafArgs a) {
+    static_assert(kGrabBlock <= 16 - S, "the next tile is needed at block 16 - S");
     using Cfg = TmaCfg<C, S, 64, CHUNK_CVS, AsyncCfg<C, S, MIS>::kUnits * 512>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t rings0 = (smem_u32(smem_raw) + 127u) & ~127u;
     const uint32_t nodes0 = rings0 + Cfg::kOffNodes;  // buffer b at nodes0 + b * kNodeBytes
     const uint32_t cvfull0 = rings0 + Cfg::kOffBars;  // 2: node buffer b is filled
     const uint32_t cvempty0 = cvfull0 + 16;           // 2: node buffer b is free
+    const uint32_t slotbar0 = cvfull0 + 32;           // kTileSlots: tile slot s is written
+    const uint32_t slots = cvfull0 + 64;              // kTileSlots tile indices
 
     const uint32_t tid = threadIdx.x;
     const uint32_t warp = tid >> 5;
@@ -572,6 +612,7 @@ __global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) l
             mbar_init(cvfull0 + 8 * b, C);
             mbar_init(cvempty0 + 8 * b, 32);
         }
+        for (uint32_t i = 0; i < kTileSlots; ++i) mbar_init(slotbar0 + 8 * i, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -581,7 +622,7 @@ __global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) l
     for (int i = 0; i < 8; ++i) key[i] = a.key[i];
 
     if (warp == Cfg::kReducerWarp) {
-        if constexpr (!CHUNK_CVS) reducer_warp<Cfg, MODE>(a, key, rings0, nodes0, cvfull0, cvempty0);
+        if constexpr (!CHUNK_CVS) reducer_warp_call<Cfg, MODE>(a, key, rings0, nodes0, cvfull0, cvempty0, slots);
         return;
     }
 
@@ -599,28 +640,32 @@ __global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) l
     const uint32_t skew = MIS ? static_cast<uint32_t>(reinterpret_cast<uintptr_t>(a.in) & 15u) : 0u;
     const uint8_t *base = a.in - skew;
 
-    // Fetch stream of this warp: fetch f brings block f mod 16 of the CTA's (f / 16)-th
-    // tile into stage f mod S; `fp` is the lane's source of the next fetch (its unit of
-    // row lrow of that tile, at that block).  The first `nfull` fetches are of tiles
-    // whose 32 rows (of this warp) are all full chunks.  Only the last tile of the input
-    // can hold other rows, and past the CTA's last tile come S fetches of no tile; those
-    // fetches copy the full-chunk rows alone, found from the row of `fp`: the other rows'
-    // CVs are discarded, or recomputed from global memory for the partial chunk.  Every
-    // fetch closes one copy group.
-    const uint64_t my_tiles = (a.n_tiles - 1 - blockIdx.x) / gridDim.x + 1;  // grid <= tiles
-    const uint64_t last_tile = blockIdx.x + (my_tiles - 1) * gridDim.x;
-    const uint32_t nfull = static_cast<uint32_t>(
-        16 * (last_tile * C + warp * 32u + 32u <= a.n_full ? my_tiles : my_tiles - 1));
-    const uint64_t jump = static_cast<uint64_t>(gridDim.x) * C * kChunkBytes - 15u * 64u;
-    const uint8_t *fp = base + (static_cast<uint64_t>(blockIdx.x) * C + lrow) * kChunkBytes + (lane >> 3) * 16u;
+    // The CTA's tiles: the first is blockIdx.x; at the start of each tile thread 0
+    // takes the next one, from the zeroed counter a.tile_counter (gridDim.x + its old
+    // value) or, without one, gridDim.x further on, and publishes it in the tile slot
+    // ring.  A tile index of n_tiles or more ends the sequence.  With the counter the
+    // tiles go to the CTAs that finish first, so every SM ends within about one tile of
+    // the others whatever the placement of the CTAs on the SMs.
+    //
+    // Fetch stream of this warp: the S blocks ahead of the one being compressed; from
+    // block 16 - S of a tile on, they are the next tile's first blocks.  `fp` is the
+    // lane's source of the next fetch (its unit of row lrow of that tile, at that
+    // block); `full_f` says whether all 32 rows of the warp in that tile are full
+    // chunks.  If not (only the input's last tile, or a tile past the end) only the
+    // full-chunk rows are copied: the other rows' CVs are discarded, or recomputed from
+    // global memory for the partial chunk.  Every fetch closes one copy group.
+    auto warp_rows_full = [&](uint64_t t) { return t * C + warp * 32u + 32u <= a.n_full; };
+    auto lane_src = [&](uint64_t t) { return base + (t * C + lrow) * kChunkBytes + (lane >> 3) * 16u; };
     // the fifth unit of the lane's own row (MIS): row warp * 32 + lane, unit 4
     const uint32_t fifth_off = (warp * 32u + lane) * static_cast<uint32_t>(kChunkBytes) + 64u -
                                (lrow * static_cast<uint32_t>(kChunkBytes) + (lane >> 3) * 16u);
     const uint32_t d5 = ring + 4u * 512u + lane * 16u;
-    uint32_t f = 0;
+    uint64_t tile = blockIdx.x;
+    const uint8_t *fp = lane_src(tile);
+    bool full_f = warp_rows_full(tile);
     auto fetch = [&](uint32_t st) {
         const uint32_t d = wr + st * Cfg::kStageBytes;
-        if (f < nfull) {
+        if (full_f) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) cp_async16(d + 128u * i, fp + 8192u * i);
             if constexpr (MIS) cp_async16(d5 + st * Cfg::kStageBytes, fp + fifth_off);
@@ -634,15 +679,15 @@ __global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) l
             }
         }
         cp_async_commit();
-        fp += (f & 15u) == 15u ? jump : 64u;
-        ++f;
+        fp += 64u;
     };
 #pragma unroll
     for (int j = 0; j < S; ++j) fetch(static_cast<uint32_t>(j));
 
     uint32_t st = 0;  // stage of the next block
-    uint32_t k = 0;
-    for (uint64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++k) {
+    bool aborted = false;
+    for (uint32_t k = 0; tile < a.n_tiles && !aborted; ++k) {
+        const uint32_t slot = k % kTileSlots;
         const uint64_t chunk = tile * C + tid;
         const uint64_t ctr = a.counter_base + chunk;
         const uint32_t ctr_lo = static_cast<uint32_t>(ctr);
@@ -658,6 +703,15 @@ __global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) l
 
 #pragma unroll 1
         for (uint32_t b = 0; b < 16; ++b) {
+            if (b == kGrabBlock && tid == 0) {
+                // the next tile, taken kGrabBlock blocks into this one: late enough that
+                // the CTAs that run faster take more tiles, early enough that the other
+                // warps find it published when they need it (block 16 - S)
+                const uint64_t nt = a.tile_counter ? gridDim.x + static_cast<uint64_t>(atomicAdd(a.tile_counter, 1u))
+                                                   : tile + gridDim.x;
+                sts64(slots + 8 * slot, nt);
+                mbar_arrive(slotbar0 + 8 * slot);
+            }
             cp_async_wait<S - 1>();  // this lane's copies of block b have landed
             __syncwarp();            // ... and every other lane's
             const uint32_t rs = rd + st * Cfg::kStageBytes;
@@ -692,13 +746,27 @@ __global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) l
             compress(cv, m, ctr_lo, ctr_hi, 64u, b == 15 ? (flags | end_flags) : flags);
             flags = MODE;
             __syncwarp();  // every lane has read stage st: refill it, S blocks ahead
+            if (b == 16 - S) {
+                // from here on the fetches are the next tile's: wait for its index
+                const bool ok = mbar_wait_bounded(slotbar0 + 8 * slot, (k / kTileSlots) & 1u, a.wait_limit_ns);
+                if (__any_sync(0xffffffffu, !ok)) {
+                    if (lane == 0) atomicOr(a.status, B3G_DEVICE_STATUS_TIMEOUT);
+                    aborted = true;
+                    break;
+                }
+                const uint64_t next = lds64(slots + 8 * slot);
+                fp = lane_src(next);
+                full_f = warp_rows_full(next);
+            }
             fetch(st);
             if (++st == S) st = 0;
         }
+        if (aborted) break;
         // the decision to leave is the warp's, so that no lane misses a warp barrier
         const bool ok = finish_tile<Cfg, CHUNK_CVS, MODE>(a, key, cv, chunk, ctr, end_flags, k, nodes0, cvfull0,
                                                           cvempty0);
         if (__any_sync(0xffffffffu, !ok)) break;
+        tile = lds64(slots + 8 * slot);  // read (after its barrier) during the last blocks
     }
     cp_async_wait<0>();  // no copy may land after the CTA has left
 }
@@ -823,7 +891,7 @@ struct Tuning<32> {
 // copies (leaf_async_kernel), 0 = bulk tensor copies (leaf_tma_kernel); and the stage
 // count of the asynchronous-copy rings per tile size.
 #ifndef B3G_STAGING
-#define B3G_STAGING 0
+#define B3G_STAGING 1
 #endif
 #ifndef B3G_ASYNC_S
 #define B3G_ASYNC_S 2
@@ -937,19 +1005,18 @@ b3g_status launch_async(const LeafArgs &a, cudaStream_t stream, int dev, const D
     return e == cudaSuccess ? B3G_OK : cuda_fail(e, "leaf_async_kernel launch");
 }
 
-// Which leaf kernel takes an input: a staged kernel for inputs with at least one full
-// chunk (the bulk-tensor-copy kernel needs a 16-byte aligned base; the asynchronous-copy
-// kernel takes any base, shifting misaligned blocks out of the aligned-down units), the
-// plain-load kernel for the rest.
+// Which leaf kernel takes an input with at least one full chunk: a 16-byte aligned base
+// goes to the staging that B3G_STAGING selects, any other base to the asynchronous-copy
+// kernel, which shifts the blocks out of the aligned-down 16-byte units (a tensor map
+// needs an aligned base).  Inputs without a full chunk take the plain-load kernel.
 enum class LeafPath { kDirect, kStaged, kStagedMisaligned };
 
 template <int C, bool CV, uint32_t MODE>
 b3g_status launch_staged(const LeafArgs &a, LeafPath path, cudaStream_t stream, int dev, const DeviceInfo &info) {
+    if (path == LeafPath::kStagedMisaligned) return launch_async<C, CV, MODE, true>(a, stream, dev, info);
 #if B3G_STAGING
-    return path == LeafPath::kStagedMisaligned ? launch_async<C, CV, MODE, true>(a, stream, dev, info)
-                                               : launch_async<C, CV, MODE, false>(a, stream, dev, info);
+    return launch_async<C, CV, MODE, false>(a, stream, dev, info);
 #else
-    (void)path;
     return launch_tma<C, CV, MODE>(a, stream, dev, info);
 #endif
 }
@@ -1008,6 +1075,12 @@ const char *kernel_config() {
     return buf;
 }
 
+bool leaf_takes_tile_counter(const void *in, uint64_t n_full) {
+    const bool full = n_full >= 1 && n_full + 256 < (1ull << 31);
+    const bool aligned = (reinterpret_cast<uintptr_t>(in) & 15u) == 0;
+    return full && (B3G_STAGING || !aligned);
+}
+
 b3g_status launch_leaf(const LeafArgs &a, int leaves_log2, bool chunk_cvs, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1020,9 +1093,7 @@ b3g_status launch_leaf(const LeafArgs &a, int leaves_log2, bool chunk_cvs, cudaS
     // base.
     const bool full = a.n_full >= 1 && a.n_full + 256 < (1ull << 31);
     const bool aligned = (reinterpret_cast<uintptr_t>(a.in) & 15u) == 0;
-    const LeafPath path = !full ? LeafPath::kDirect
-                          : aligned ? LeafPath::kStaged
-                                    : (B3G_STAGING ? LeafPath::kStagedMisaligned : LeafPath::kDirect);
+    const LeafPath path = !full ? LeafPath::kDirect : aligned ? LeafPath::kStaged : LeafPath::kStagedMisaligned;
     switch (leaves_log2) {
         case 5: return launch_c<32>(a, chunk_cvs, path, stream, dev, info);
         case 6: return launch_c<64>(a, chunk_cvs, path, stream, dev, info);

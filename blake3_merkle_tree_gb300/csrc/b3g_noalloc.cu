@@ -110,6 +110,7 @@ extern "C" b3g_status blake3_keyed_hash_noalloc(const void *d_in, uint64_t len, 
     a.tail_bytes = static_cast<uint32_t>(len % kChunkBytes);
     a.ticket = nullptr;
     a.final_out = nullptr;
+    a.tile_counter = nullptr;
     if (tiles == 1) {
         a.out = d_out32;
         return launch_leaf(a, t, false, s);

@@ -46,10 +46,20 @@ def shard_range(total_len: int, world: int, rank: int) -> tuple[int, int]:
     return min(t0 * TILE_BYTES, total_len), min(t1 * TILE_BYTES, total_len)
 
 
+_counters = {}
+
+
 def _device_tile_roots(data, key, chunk_offset, is_root, out):
+    """The rank's tile roots, the tiles taken from a counter zeroed on the current
+    stream (dynamic scheduling: the CTAs that run faster take more tiles)."""
     from . import binding
 
-    return binding.blake3_keyed_tile_roots(data, key, chunk_offset, TILE_LOG2, is_root, out)
+    dev = out.device
+    if dev not in _counters:
+        _counters[dev] = torch.zeros(4, dtype=torch.int32, device=dev)
+    counter = _counters[dev]
+    counter.zero_()
+    return binding.blake3_keyed_tile_roots(data, key, chunk_offset, TILE_LOG2, is_root, out, tile_counter=counter)
 
 
 def _device_fold(cvs, key, out, workspace):

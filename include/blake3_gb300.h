@@ -207,6 +207,24 @@ b3g_status blake3_keyed_tile_roots(const void *d_in, uint64_t len, uint64_t chun
                                    const uint8_t key[32], int leaves_log2, int is_root,
                                    uint8_t *d_roots, b3g_stream_t stream);
 
+/*
+ * blake3_keyed_tile_roots_ex -- as blake3_keyed_tile_roots, with dynamic tile
+ * scheduling.  d_tile_counter is a 4-byte aligned DEVICE word that the caller has set
+ * to zero on `stream` before the call (or NULL: the static order of
+ * blake3_keyed_tile_roots).  After its first tile each persistent CTA takes its next
+ * tile from the counter, so CTAs that run faster take more tiles and all of them
+ * finish together; the warp scheduler favours some CTAs of an SM over others, which
+ * leaves a static split with idle warps in its second half.  The roots are the same
+ * either way.  The counter is used only by the asynchronous-copy leaf kernel (see
+ * blake3_kernel_config); the other kernels ignore it.  One counter serves one call at
+ * a time.  Scheduling only; the page's Kernel 1 assigns tiles statically.
+ * Errors: as blake3_keyed_tile_roots, plus B3G_ERR_ALIGN (d_tile_counter).
+ */
+b3g_status blake3_keyed_tile_roots_ex(const void *d_in, uint64_t len, uint64_t chunk_offset,
+                                      const uint8_t key[32], int leaves_log2, int is_root,
+                                      uint8_t *d_roots, uint32_t *d_tile_counter,
+                                      b3g_stream_t stream);
+
 /* Device workspace bytes blake3_keyed_reduce_cvs needs for `count` CVs and groups of
  * 2^group_log2 (group_log2 in 1..10, or -1 for the default: 6 for at most 32,768 CVs,
  * else 10). */

@@ -67,10 +67,14 @@ def test_sizes(lib):
     assert lib.blake3_workspace_size(19 << 20) == 152 * 32 + 3 * 32  # 19456 chunks / 128
     # 144 tiles of 128 < 152: 64-chunk tiles, 288 -> 5 -> 1
     assert lib.blake3_workspace_size(18 << 20) == 288 * 32 + 5 * 32
-    # 4 GiB: 32768 tile CVs, then 512 and 8 group CVs
-    assert lib.blake3_workspace_size(1 << 32) == 32768 * 32 + 512 * 32 + 8 * 32
+    # 4 GiB: 32768 tile CVs, then 512 and 8 group CVs, then 16 bytes for the tile counter
+    # (more tiles than one per resident CTA)
+    assert lib.blake3_workspace_size(1 << 32) == 32768 * 32 + 512 * 32 + 8 * 32 + 16
     # 12 GiB + 777: 98305 tile CVs, groups of 1024 above 32,768 CVs: 97 group CVs
-    assert lib.blake3_workspace_size(12 * (1 << 30) + 777) == 98305 * 32 + 97 * 32
+    assert lib.blake3_workspace_size(12 * (1 << 30) + 777) == 98305 * 32 + 97 * 32 + 16
+    # 760 tiles of 128 chunks: no counter; 761: a counter
+    assert lib.blake3_workspace_size(760 * 128 * 1024) == 760 * 32 + 12 * 32
+    assert lib.blake3_workspace_size(760 * 128 * 1024 + 1) == 761 * 32 + 12 * 32 + 16
     assert lib.blake3_reduce_workspace_size(1024, 10) == 0
     assert lib.blake3_reduce_workspace_size(1025, 10) == 64
     assert lib.blake3_reduce_workspace_size(5, 1) == 3 * 32 + 32 + 32

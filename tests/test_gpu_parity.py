@@ -209,3 +209,30 @@ def test_every_misalignment_residue(r):
     assert bytes(binding.blake3_hash(x).cpu().numpy()) == oracle.hash(ref)
     cvs = binding.blake3_keyed_chunk_cvs(x, KEY).cpu().numpy()
     assert (cvs == oracle.chunk_cvs(ref, KEY)).all()
+
+
+@pytest.mark.parametrize("offset", [0, 5])
+def test_dynamic_tile_schedule_gives_the_static_roots(offset):
+    """Tiles taken from a zeroed counter (more tiles than resident CTAs, ragged tail,
+    aligned and misaligned) give the same roots as the static order, and those roots are
+    the oracle's subtree CVs; every tile is taken exactly once."""
+    n = 200 * (1 << 20) + 777
+    host = workloads.uniform_bytes(31, n)
+    buf = torch.empty(n + offset, dtype=torch.uint8, device="cuda")
+    buf[offset:].copy_(host)
+    dev = buf[offset:]
+    tiles = binding.blake3_tile_count(n, -1)
+    assert tiles > 760
+    static = binding.blake3_keyed_tile_roots(dev, KEY)
+    counter = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        counter.zero_()
+        dyn = binding.blake3_keyed_tile_roots(dev, KEY, tile_counter=counter)
+        assert torch.equal(dyn, static)
+        if binding.library().blake3_kernel_config().startswith(b"leaf_async_kernel") or offset:
+            assert int(counter.item()) == tiles  # one take per tile processed, then none left
+    roots = static.cpu().numpy()
+    per = 128 * 1024
+    for t in (0, 1, 759, 760, 761, tiles - 2, tiles - 1):
+        want = oracle.subtree_cv(host[t * per:min(n, (t + 1) * per)], KEY, t * 128)
+        assert bytes(roots[t]) == want, t
