@@ -40,7 +40,8 @@ WORKLOAD = "12GiB+777"
 # x 12 operations (6 adds with the two 3-input adds fused, 4 XORs, 4 rotates ->
 # 2 IADD3 + 2 IADD + 4 XOR + 4 rotates) + 8 XORs for the output CV.
 OPS_PER_COMPRESSION = 7 * 8 * 12 + 8
-# The page's count ("7 rounds x 8 G x 6 operations = 336 per 64-byte block").
+# The page's count: 6 operations per G, 336 per 64-byte block ("BLAKE3 GPU 400x faster hashing",
+# section "压缩函数").
 PAGE_OPS_PER_COMPRESSION = 336
 DYNAMIC_MIN_TILES = 760  # above this many CTA subtrees the leaf kernel takes tiles from a counter
 INT32_LANES_PER_SM = 128  # integer instructions issued per SM per clock (4 schedulers x 32 lanes)
@@ -118,15 +119,20 @@ class ClockSampler:
 
 def _traffic_per_launch(lib, nchunks):
     """DRAM bytes and issued thread instructions of one leaf launch, scaled by chunks from
-    the ncu capture recorded in profiles/leaf_tma_kernel_traffic.json; None if that
-    capture is of another kernel configuration than the one built."""
-    p = os.path.join(HERE, "profiles", "leaf_tma_kernel_traffic.json")
-    if not os.path.exists(p):
-        return None, None, None
-    with open(p) as f:
-        rec = json.load(f)
-    if rec.get("kernel_config") != lib.blake3_kernel_config().decode():
-        return None, "capture is of another kernel configuration", None
+    the ncu capture recorded in profiles/leaf_*_traffic.json for the kernel configuration
+    built; None if there is none."""
+    cfg = lib.blake3_kernel_config().decode()
+    rec = None
+    for name in ("leaf_async_kernel_traffic.json", "leaf_tma_kernel_traffic.json"):
+        p = os.path.join(HERE, "profiles", name)
+        if os.path.exists(p):
+            with open(p) as f:
+                r = json.load(f)
+            if r.get("kernel_config") == cfg:
+                rec = r
+                break
+    if rec is None:
+        return None, "no capture of this kernel configuration", None
     per_chunk = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) / rec["chunks"]
     issued = None
     if "warp_inst_executed" in rec:

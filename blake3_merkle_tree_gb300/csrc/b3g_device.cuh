@@ -246,9 +246,13 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
     return ok != 0;
 }
 
-// Suspend-time hint of the bounded waits (0: none, the hardware's own limit).
+// Suspend-time hint of the bounded waits (0: none, the hardware's own limit).  Without
+// it the reducer warp, idle most of the time, polls its barrier and takes issue slots
+// from the consumers; with a hint it sleeps until the phase completes.  Measured (leaf
+// kernel, GB/s): 12 GiB + 777 B 2223 -> 2261, 4 GiB 2180 -> 2219, 256 MiB 1839 -> 1859,
+// the same with 1 us and 20 us.
 #ifndef B3G_WAIT_HINT_NS
-#define B3G_WAIT_HINT_NS 0
+#define B3G_WAIT_HINT_NS 20000
 #endif
 
 __device__ __forceinline__ uint64_t global_timer_ns() {

@@ -1059,10 +1059,11 @@ const char *kernel_config() {
     std::call_once(once, [] {
 #if B3G_STAGING
         std::snprintf(buf, sizeof buf,
-                      "leaf_async_kernel<%d,%d> min_blocks=%d g_form=%d top_batch=%d pair_noinline=%d "
-                      "rot_fma=0x%x pdl=1 modes=2",
-                      1 << kDefaultLeavesLog2, AsyncTuning<(1 << kDefaultLeavesLog2)>::S, B3G_MIN_BLOCKS,
-                      B3G_G_FORM, B3G_TOP_BATCH, B3G_PAIR_NOINLINE, static_cast<unsigned>(B3G_ROT_FMA));
+                      "leaf_async_kernel<%d,%d> min_blocks=%d g_form=%d top_batch=%d grab_block=%d "
+                      "wait_hint_ns=%d rot_fma=0x%x pdl=1 modes=2",
+                      1 << kDefaultLeavesLog2, AsyncTuning<(1 << kDefaultLeavesLog2)>::S, B3G_ASYNC_MIN_BLOCKS,
+                      B3G_G_FORM, B3G_TOP_BATCH, B3G_GRAB_BLOCK, B3G_WAIT_HINT_NS,
+                      static_cast<unsigned>(B3G_ROT_FMA));
 #else
         std::snprintf(buf, sizeof buf,
                       "leaf_tma_kernel<%d,%d,%d> unroll=%d min_blocks=%d g_form=%d top_batch=%d pair_noinline=%d "
