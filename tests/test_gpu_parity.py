@@ -236,3 +236,23 @@ def test_dynamic_tile_schedule_gives_the_static_roots(offset):
     for t in (0, 1, 759, 760, 761, tiles - 2, tiles - 1):
         want = oracle.subtree_cv(host[t * per:min(n, (t + 1) * per)], KEY, t * 128)
         assert bytes(roots[t]) == want, t
+
+
+@pytest.mark.parametrize("tiles,offset", [(761, 0), (4097, 0), (761, 3)])
+def test_one_shot_digest_with_tile_counter(tiles, offset):
+    """Above 760 tiles the one-shot digest takes tiles from a counter that it zeroes in its
+    workspace (761 tiles: two reduction levels, 4097: three).  A dirty workspace, reused
+    call after call, gives the oracle's digest, keyed and in the default mode, aligned and
+    misaligned."""
+    n = tiles * 128 * 1024 - 5000  # a partial last tile and a partial last chunk
+    host = workloads.uniform_bytes(tiles, n)
+    buf = torch.empty(n + offset, dtype=torch.uint8, device="cuda")
+    buf[offset:].copy_(host)
+    dev = buf[offset:]
+    want = oracle.keyed_hash(host, KEY)
+    ws = torch.full((binding.blake3_workspace_size(n),), 0xA5, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        assert bytes(binding.blake3_keyed_hash_ws(dev, KEY, ws).cpu().numpy()) == want
+    assert bytes(binding.blake3_keyed_hash(dev, KEY).cpu().numpy()) == want
+    if tiles == 761 and offset == 0:
+        assert bytes(binding.blake3_hash_ws(dev, ws).cpu().numpy()) == oracle.hash(host)
