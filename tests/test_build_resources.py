@@ -29,12 +29,12 @@ _ASYNC = re.compile(r"leaf_async_kernelILi(\d+)ELi(\d+)ELb([01])ELj(\d+)ELb([01]
 _ASYNC_MAX_SPILL_LOADS_MISALIGNED = 28
 
 
-def _ptxas_report(tmp_path):
+def _ptxas_report(tmp_path, extra=()):
     nvcc = build.nvcc()
     if not (os.path.exists(nvcc) or shutil.which(nvcc)):
         pytest.skip("nvcc not available")
     obj = tmp_path / "leaf.o"
-    cmd = [nvcc, *build._flags(True), "-c", os.path.join(build.CSRC, "b3g_leaf.cu"), "-o", str(obj)]
+    cmd = [nvcc, *build._flags(True), *extra, "-c", os.path.join(build.CSRC, "b3g_leaf.cu"), "-o", str(obj)]
     p = subprocess.run(cmd, capture_output=True, text=True)
     assert p.returncode == 0, p.stderr[-4000:]
     kernels = {}
@@ -55,8 +55,11 @@ def _ptxas_report(tmp_path):
     return kernels
 
 
-def test_leaf_kernels_keep_five_ctas_per_sm(tmp_path):
-    kernels = _ptxas_report(tmp_path)
+@pytest.mark.parametrize("staging", ["default", "tma"])
+def test_leaf_kernels_keep_five_ctas_per_sm(tmp_path, staging):
+    """The default build (asynchronous copies for every staged input) and the build with
+    the bulk-tensor-copy staging for aligned inputs (B3G_STAGING=0), which stays buildable."""
+    kernels = _ptxas_report(tmp_path, ["-DB3G_STAGING=0"] if staging == "tma" else [])
     tma = asy = 0
     for name, (regs, (_, spill_loads)) in kernels.items():
         m = _TMA.search(name)
@@ -75,3 +78,4 @@ def test_leaf_kernels_keep_five_ctas_per_sm(tmp_path):
     # one staging for aligned inputs (keyed and default mode, with and without the chunk-CV
     # output) and the asynchronous-copy kernel for misaligned ones (the same three)
     assert tma + asy == 6 and asy >= 3, sorted(kernels)
+    assert tma == (3 if staging == "tma" else 0)
