@@ -583,14 +583,15 @@ __device__ __forceinline__ void shifted_words(const uint32_t x[20], uint32_t sh,
     for (int i = 0; i < 16; ++i) m[i] = __funnelshift_r(x[i + Q], x[i + Q + 1], sh);
 }
 
-// Block of a tile at which thread 0 takes the CTA's next tile from the counter.
+// Block of a tile at which thread 0 takes the CTA's next tile from the counter (-1: at
+// block 16 - S, the first one whose refill is the next tile's).
 #ifndef B3G_GRAB_BLOCK
-#define B3G_GRAB_BLOCK 14
+#define B3G_GRAB_BLOCK -1
 #endif
-constexpr uint32_t kGrabBlock = B3G_GRAB_BLOCK;
 
 template <int C, int S, bool CHUNK_CVS, uint32_t MODE, bool MIS>
 __global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) leaf_async_kernel(const LeafArgs a) {
+    constexpr uint32_t kGrabBlock = B3G_GRAB_BLOCK < 0 ? 16 - S : B3G_GRAB_BLOCK;
     static_assert(kGrabBlock <= 16 - S, "the next tile is needed at block 16 - S");
     using Cfg = TmaCfg<C, S, 64, CHUNK_CVS, AsyncCfg<C, S, MIS>::kUnits * 512>;
     extern __shared__ uint8_t smem_raw[];
@@ -1062,7 +1063,9 @@ const char *kernel_config() {
                       "leaf_async_kernel<%d,%d> min_blocks=%d g_form=%d top_batch=%d grab_block=%d "
                       "wait_hint_ns=%d rot_fma=0x%x pdl=1 modes=2",
                       1 << kDefaultLeavesLog2, AsyncTuning<(1 << kDefaultLeavesLog2)>::S, B3G_ASYNC_MIN_BLOCKS,
-                      B3G_G_FORM, B3G_TOP_BATCH, B3G_GRAB_BLOCK, B3G_WAIT_HINT_NS,
+                      B3G_G_FORM, B3G_TOP_BATCH,
+                      B3G_GRAB_BLOCK < 0 ? 16 - AsyncTuning<(1 << kDefaultLeavesLog2)>::S : B3G_GRAB_BLOCK,
+                      B3G_WAIT_HINT_NS,
                       static_cast<unsigned>(B3G_ROT_FMA));
 #else
         std::snprintf(buf, sizeof buf,
