@@ -646,7 +646,9 @@ __global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) l
     // value) or, without one, gridDim.x further on, and publishes it in the tile slot
     // ring.  A tile index of n_tiles or more ends the sequence.  With the counter the
     // tiles go to the CTAs that finish first, so every SM ends within about one tile of
-    // the others whatever the placement of the CTAs on the SMs.
+    // the others whatever the placement of the CTAs on the SMs.  Every tile processed
+    // takes once (the CTA's last take finds no tile), so a launch that completes takes
+    // exactly n_tiles times and the last take leaves the counter at zero again.
     //
     // Fetch stream of this warp: the S blocks ahead of the one being compressed; from
     // block 16 - S of a tile on, they are the next tile's first blocks.  `fp` is the
@@ -708,8 +710,14 @@ __global__ void __launch_bounds__(C + 32, C == 128 ? B3G_ASYNC_MIN_BLOCKS : 1) l
                 // the next tile, taken kGrabBlock blocks into this one: late enough that
                 // the CTAs that run faster take more tiles, early enough that the other
                 // warps find it published when they need it (block 16 - S)
-                const uint64_t nt = a.tile_counter ? gridDim.x + static_cast<uint64_t>(atomicAdd(a.tile_counter, 1u))
-                                                   : tile + gridDim.x;
+                uint64_t nt = tile + gridDim.x;
+                if (a.tile_counter) {
+                    // one take per tile processed, n_tiles in all: the take that returns
+                    // n_tiles - 1 is the last, and puts the counter back to zero
+                    const uint32_t old = atomicAdd(a.tile_counter, 1u);
+                    if (old == static_cast<uint32_t>(a.n_tiles - 1)) atomicExch(a.tile_counter, 0u);
+                    nt = gridDim.x + static_cast<uint64_t>(old);
+                }
                 sts64(slots + 8 * slot, nt);
                 mbar_arrive(slotbar0 + 8 * slot);
             }

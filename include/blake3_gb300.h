@@ -143,8 +143,8 @@ b3g_status blake3_keyed_hash_ws(const void *d_in, uint64_t len, const uint8_t ke
  * `stream` after it, without synchronising the device or touching other streams' calls
  * (the caller zeroes the word before the call, or keeps ORing several calls into it).
  * With the word clear the digest in d_out32 is valid; with the bit set it is not.
- * Failure detection of the leaf and reduction kernels (SURVEY: failure detection);
- * the page has no counterpart.
+ * It is the failure detection of the leaf and reduction kernels, and has no
+ * counterpart in the page.
  * Errors: as blake3_keyed_hash_ws, plus B3G_ERR_NULL (d_status NULL) and
  * B3G_ERR_ALIGN (d_status not 4-byte aligned).
  */
@@ -217,7 +217,11 @@ b3g_status blake3_keyed_tile_roots(const void *d_in, uint64_t len, uint64_t chun
  * leaves a static split with idle warps in its second half.  The roots are the same
  * either way.  The counter is used only by the asynchronous-copy leaf kernel (see
  * blake3_kernel_config); the other kernels ignore it.  One counter serves one call at
- * a time.  Scheduling only; the page's Kernel 1 assigns tiles statically.
+ * a time.  A call whose kernels complete without a given-up wait leaves the counter at
+ * zero again (the CTAs take from it exactly once per tile, and the last take resets
+ * it), so a caller that reuses the counter for calls in stream order clears it once;
+ * after a call that reported B3G_DEVICE_STATUS_TIMEOUT it must be cleared again.
+ * Scheduling only; the page's Kernel 1 assigns tiles statically.
  * Errors: as blake3_keyed_tile_roots, plus B3G_ERR_ALIGN (d_tile_counter).
  */
 b3g_status blake3_keyed_tile_roots_ex(const void *d_in, uint64_t len, uint64_t chunk_offset,
