@@ -117,22 +117,38 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows), "samples": len(loaded), "reasons": reasons}
 
 
+def _leaf_sources_sha256() -> str:
+    """SHA-256 (first 16 hex digits) of the sources the leaf kernels are built from: a
+    counter capture holds for the kernel only while these are unchanged."""
+    import hashlib
+
+    csrc = os.path.join(HERE, "blake3_merkle_tree_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("b3g_leaf.cu", "b3g_device.cuh", "b3g_internal.h"):
+        h.update(name.encode())
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def _traffic_per_launch(lib, nchunks):
     """DRAM bytes and issued thread instructions of one leaf launch, scaled by chunks from
     the ncu capture recorded in profiles/leaf_*_traffic.json for the kernel configuration
-    built; None if there is none."""
+    built and the leaf sources as they are; None if there is none (the kernel changed
+    since the counters were taken)."""
     cfg = lib.blake3_kernel_config().decode()
+    src = _leaf_sources_sha256()
     rec = None
     for name in ("leaf_async_kernel_traffic.json", "leaf_tma_kernel_traffic.json"):
         p = os.path.join(HERE, "profiles", name)
         if os.path.exists(p):
             with open(p) as f:
                 r = json.load(f)
-            if r.get("kernel_config") == cfg:
+            if r.get("kernel_config") == cfg and r.get("leaf_sources_sha256") == src:
                 rec = r
                 break
     if rec is None:
-        return None, "no capture of this kernel configuration", None
+        return None, "no capture of this kernel configuration and these leaf sources", None
     per_chunk = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) / rec["chunks"]
     issued = None
     if "warp_inst_executed" in rec:
