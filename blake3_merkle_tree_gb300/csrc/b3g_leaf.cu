@@ -61,18 +61,17 @@
 #define B3G_LEAF_BOUNDS(threads) __launch_bounds__(threads)
 #endif
 // Full tiles whose top tree levels the reducer warp runs together (0: every tile on
-// its own), and whether the reducer's tree level is a called function (1) or inlined
-// at each use (0).
+// its own), and whether the asynchronous-copy kernel's reducer runs each tree level as
+// a called function (1) or inlined at each use (0).  As a call, that reducer holds one
+// copy of the compression for all its levels instead of one per use: its code stays in
+// the instruction caches, and the tree work that ends each launch runs sooner.  The
+// bulk-tensor-copy kernel keeps the inlined levels (as a call its reducer would need 95
+// registers, one CTA per SM fewer).
 #ifndef B3G_TOP_BATCH
 #define B3G_TOP_BATCH 8
 #endif
 #ifndef B3G_PAIR_NOINLINE
-#define B3G_PAIR_NOINLINE 0
-#endif
-#if B3G_PAIR_NOINLINE
-#define B3G_PAIR_ATTR __noinline__
-#else
-#define B3G_PAIR_ATTR __forceinline__
+#define B3G_PAIR_NOINLINE 1
 #endif
 
 namespace b3g {
@@ -166,7 +165,8 @@ __device__ __noinline__ Words8 partial_chunk_cv(const uint8_t *in, uint64_t len,
 
 // One tree level in shared memory: node j of `dst` = parent(node 2j, node 2j+1 of
 // `src`) for j < half, the lanes of the calling warp striding over j.
-__device__ B3G_PAIR_ATTR void pair_level(uint32_t src, uint32_t dst, uint32_t half, Words8 key, uint32_t mode_flags) {
+__device__ __forceinline__ void pair_level_inline(uint32_t src, uint32_t dst, uint32_t half, Words8 key,
+                                                  uint32_t mode_flags) {
     const uint32_t lane = threadIdx.x & 31u;
     for (uint32_t j = lane; j < half; j += 32) {
         uint32_t l[8], r[8], p[8];
@@ -175,6 +175,22 @@ __device__ B3G_PAIR_ATTR void pair_level(uint32_t src, uint32_t dst, uint32_t ha
         parent(key.w, mode_flags, l, r, false, p);
         store_node(dst, j, p);
     }
+}
+
+// The same level as a called function.
+__device__ __noinline__ void pair_level_call(uint32_t src, uint32_t dst, uint32_t half, Words8 key,
+                                             uint32_t mode_flags) {
+    pair_level_inline(src, dst, half, key, mode_flags);
+}
+
+// The level as the reducer of configuration CALL runs it.
+template <bool CALL>
+__device__ __forceinline__ void pair_level(uint32_t src, uint32_t dst, uint32_t half, Words8 key,
+                                           uint32_t mode_flags) {
+    if constexpr (CALL)
+        pair_level_call(src, dst, half, key, mode_flags);
+    else
+        pair_level_inline(src, dst, half, key, mode_flags);
 }
 
 // Fused final reduction (at most 32 tiles, one tile per CTA).  Called by a whole
@@ -223,7 +239,7 @@ constexpr uint32_t kTileSlots = 4;
 // published in the tile index ring at `slots` (the first is blockIdx.x): the tile after
 // the k-th was published before the consumers' hand-over of the k-th, which the reducer
 // has waited for, so reading it needs no further wait.
-template <typename Cfg, uint32_t MODE>
+template <typename Cfg, uint32_t MODE, bool PAIR_CALL = false>
 __device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t key[8], uint32_t rings0,
                                              uint32_t nodes0, uint32_t cvfull0, uint32_t cvempty0,
                                              uint32_t slots = 0) {
@@ -247,7 +263,7 @@ __device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t k
         if (pending == 0) return;
         uint32_t n = pending * 32u, src = topA, dst = topB;
         while (n > pending) {
-            pair_level(src, dst, n >> 1, key8, MODE);
+            pair_level<PAIR_CALL>(src, dst, n >> 1, key8, MODE);
             __syncwarp();
             const uint32_t t = src;
             src = dst;
@@ -280,7 +296,7 @@ __device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t k
             uint32_t src = src0, level = 0;
             for (uint32_t n = C; n > 32; n >>= 1, ++level) {
                 const uint32_t dst = n == 64 ? slot : ((level & 1u) ? scratch2 : scratch1);
-                pair_level(src, dst, n >> 1, key8, MODE);
+                pair_level<PAIR_CALL>(src, dst, n >> 1, key8, MODE);
                 __syncwarp();
                 if (level == 0) mbar_arrive(cvempty0 + 8 * b);  // node buffer read
                 src = dst;
@@ -308,7 +324,7 @@ __device__ __forceinline__ void reducer_warp(const LeafArgs &a, const uint32_t k
         while (cnt > 32) {
             const uint32_t dst = (level & 1u) ? scratch2 : scratch1;
             const uint32_t half = cnt >> 1;
-            pair_level(src, dst, half, key8, MODE);
+            pair_level<PAIR_CALL>(src, dst, half, key8, MODE);
             if ((cnt & 1u) && lane == 0) {
                 uint32_t t[8];
                 load_node(src, cnt - 1, t);
@@ -347,7 +363,7 @@ __device__ __noinline__ void reducer_warp_call(const LeafArgs &a, const uint32_t
     uint32_t k8[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) k8[i] = key[i];
-    reducer_warp<Cfg, MODE>(a, k8, rings0, nodes0, cvfull0, cvempty0, slots);
+    reducer_warp<Cfg, MODE, B3G_PAIR_NOINLINE != 0>(a, k8, rings0, nodes0, cvfull0, cvempty0, slots);
 }
 
 // End of a consumer thread's tile: the owner of the partial last chunk redoes it from
@@ -1068,10 +1084,10 @@ const char *kernel_config() {
     std::call_once(once, [] {
 #if B3G_STAGING
         std::snprintf(buf, sizeof buf,
-                      "leaf_async_kernel<%d,%d> min_blocks=%d g_form=%d top_batch=%d grab_block=%d "
+                      "leaf_async_kernel<%d,%d> min_blocks=%d g_form=%d top_batch=%d pair_noinline=%d grab_block=%d "
                       "wait_hint_ns=%d rot_fma=0x%x pdl=1 modes=2",
                       1 << kDefaultLeavesLog2, AsyncTuning<(1 << kDefaultLeavesLog2)>::S, B3G_ASYNC_MIN_BLOCKS,
-                      B3G_G_FORM, B3G_TOP_BATCH,
+                      B3G_G_FORM, B3G_TOP_BATCH, B3G_PAIR_NOINLINE,
                       B3G_GRAB_BLOCK < 0 ? 16 - AsyncTuning<(1 << kDefaultLeavesLog2)>::S : B3G_GRAB_BLOCK,
                       B3G_WAIT_HINT_NS,
                       static_cast<unsigned>(B3G_ROT_FMA));
