@@ -24,13 +24,16 @@
 namespace b3g {
 namespace {
 
-// 65,536 CTA roots (16 GiB of input at 256 chunks per CTA) plus the 64 CVs of the
-// next reduction level, rounded up.
-constexpr size_t kNoAllocScratchBytes = (2u << 20) + 4096;
-// Inputs above 2^16 chunks (64 MiB) use 256 chunks per CTA subtree: the scratch size
-// above is computed for it.  Smaller inputs use the one-shot digest's subtree size
-// (down to 32 chunks, so that every SM gets a CTA), at most 2048 roots.
-constexpr int kNoAllocLeavesLog2 = 8;
+// 131,072 CTA roots (16 GiB of input at 128 chunks per CTA), the reduction levels
+// after them (128 CVs with groups of 1024; at most 520 with groups of 64, which serve
+// up to 32,768 roots) and, in the last 16 bytes, the leaf kernel's tile counter.
+constexpr size_t kNoAllocScratchBytes = (4u << 20) + 8192;
+constexpr size_t kNoAllocCounterOffset = kNoAllocScratchBytes - 16;
+// Inputs above 2^16 chunks (64 MiB) use 128 chunks per CTA subtree, as the one-shot
+// digest does: the scratch size above is computed for it.  Smaller inputs use the
+// one-shot digest's subtree size (down to 32 chunks, so that every SM gets a CTA), at
+// most 2048 roots.
+constexpr int kNoAllocLeavesLog2 = kDefaultLeavesLog2;
 constexpr uint64_t kNoAllocSmallChunks = 1ull << 16;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
@@ -76,15 +79,16 @@ extern "C" b3g_status blake3_keyed_hash_noalloc(const void *d_in, uint64_t len, 
     const uint64_t n_chunks = len == 0 ? 1 : ceil_div(len, kChunkBytes);
     const int t = n_chunks <= kNoAllocSmallChunks ? leaves_log2_for(n_chunks) : kNoAllocLeavesLog2;
     const uint64_t tiles = ceil_div(n_chunks, 1ull << t);
-    const uint64_t group = 1ull << kDefaultGroupLog2;
+    const uint64_t group = 1ull << reduce_group_log2(tiles);
 
-    // scratch layout: the CTA roots, then one buffer per further reduction level
+    // scratch layout: the CTA roots, then one buffer per further reduction level; the
+    // tile counter at its end
     size_t need = tiles > 1 ? round16(tiles * 32) : 0;
     for (uint64_t c = tiles; c > group;) {
         c = ceil_div(c, group);
         need += round16(c * 32);
     }
-    if (need > kNoAllocScratchBytes) return B3G_ERR_WORKSPACE;
+    if (need > kNoAllocCounterOffset) return B3G_ERR_WORKSPACE;
 
     uint32_t *status = nullptr;
     b3g_status st = device_status_word(&status);
@@ -116,9 +120,14 @@ extern "C" b3g_status blake3_keyed_hash_noalloc(const void *d_in, uint64_t len, 
         return launch_leaf(a, t, false, s);
     }
     // Every CTA root and every level buffer is written before it is read within this
-    // call, so nothing left in the scratch by an earlier call is ever used and no
-    // clearing is needed.
+    // call, so nothing left in the scratch by an earlier call is ever used.  Only the
+    // tile counter (more tiles than resident CTAs) is cleared first.
     a.out = scratch;
+    if (tiles > kDynamicMinTiles && leaf_takes_tile_counter(d_in, a.n_full)) {
+        a.tile_counter = reinterpret_cast<uint32_t *>(scratch + kNoAllocCounterOffset);
+        const cudaError_t e = cudaMemsetAsync(a.tile_counter, 0, sizeof(uint32_t), s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(noalloc tile counter)");
+    }
     st = launch_leaf(a, t, false, s);
     if (st != B3G_OK) return st;
     const uint8_t *cur = scratch;

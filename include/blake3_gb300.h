@@ -419,16 +419,17 @@ b3g_status blake3_hash_host(const void *h_in, uint64_t len, uint8_t out32[32], v
 
 /*
  * blake3_keyed_hash_noalloc -- the same digest as blake3_keyed_hash, computed without
- * allocating any device memory.  The paper has no counterpart to this entry point.
+ * allocating any device memory.  The page has no counterpart to this entry point.
  *
  * For callers that cannot allocate device memory when they hash: for example a
  * process whose GPU memory is already owned by another allocator (a framework's
  * caching allocator), a latency-critical loop that cannot accept the device-wide
  * synchronisation cudaMalloc/cudaFree may cause, or a service that forbids allocation
- * after start-up.  The CTA roots are kept in a fixed scratch array of 2 MiB + 4 KiB
- * that is part of the library's device image: every GPU that loads libb3g.so holds it
- * until the process exits.  The caller still provides the input and the 32-byte,
- * 16-byte aligned output.
+ * after start-up.  The CTA roots and the leaf kernel's tile counter are kept in a
+ * fixed scratch array of 4 MiB + 8 KiB that is part of the library's device image:
+ * every GPU that loads libb3g.so holds it until the process exits.  The caller still
+ * provides the input and the 32-byte, 16-byte aligned output.  The kernels and CTA
+ * subtree sizes are those of blake3_keyed_hash.
  *
  * Limits and rules:
  *   - len may be at most B3G_NOALLOC_MAX_LEN (16 GiB); a larger input returns
@@ -439,8 +440,9 @@ b3g_status blake3_hash_host(const void *h_in, uint64_t len, uint8_t out32[32], v
  *   - All calls share the one scratch array, and it keeps the last call's contents.
  *     Calls whose work overlaps on the GPU (concurrent streams, or several host
  *     threads on one device) race on it and give wrong digests; serialise them.
- *     Within one call everything read from the scratch is written first, so
- *     leftovers of an earlier call do no harm.
+ *     Within one call everything read from the scratch is written first (the tile
+ *     counter is cleared with a memset on `stream`), so leftovers of an earlier call
+ *     do no harm.
  * Errors: B3G_ERR_NULL, B3G_ERR_ALIGN (d_out32), B3G_ERR_WORKSPACE (len too large),
  * B3G_ERR_CUDA.
  */

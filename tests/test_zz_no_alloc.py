@@ -6,8 +6,9 @@ start-up).  It keeps its CTA roots in a fixed scratch array inside the library.
 Checked through the C ABI against the CPU oracle and against blake3_keyed_hash, call
 after call (each call reuses the scratch the one before left behind), over every path
 the entry point can take: the empty input, inputs shorter than a chunk and than a CTA
-subtree (no scratch used), the small-input subtree sizes, a misaligned view (the
-plain-load kernel), and an input of more than 1024 CTA subtrees (two reduction levels).
+subtree (no scratch used), the small-input subtree sizes, a misaligned view, and an
+input of more than 760 CTA subtrees (the tile counter in the scratch, two reduction
+levels).
 This file is collected last on purpose."""
 
 import ctypes
@@ -33,7 +34,8 @@ def _noalloc(lib, dev, key):
 
 # (length, byte offset of the view): 0, 1 and 1023 bytes fit one CTA subtree; 5 MiB + 3
 # takes the small-input subtree size; 9 MiB + 5 at offset 3 is misaligned; 300 MiB + 777
-# is 1201 subtrees of 256 chunks (two reduction levels)
+# is 2401 subtrees of 128 chunks (more than one per resident CTA: the tile counter; two
+# reduction levels)
 CASES = [(0, 0), (1, 0), (1023, 0), (5 * (1 << 20) + 3, 0), (9 * (1 << 20) + 5, 3), (300 * (1 << 20) + 777, 0)]
 
 
