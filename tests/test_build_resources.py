@@ -9,9 +9,10 @@ leaf kernels with the package's own flags and reads ptxas's resource report.
 - The bulk-tensor-copy kernel (leaf_tma_kernel) compiles to 72 registers without spill
   loads.
 - The asynchronous-copy kernel (leaf_async_kernel) is held to five CTAs by its launch
-  bounds and calls its reducer warp as a function.  The aligned kernels then spill
-  nothing.  The misaligned ones (one more 16-byte unit and a shift per block) reload up
-  to 28 bytes; the test caps them there.
+  bounds and calls its reducer warp as a function (which calls its tree level in turn;
+  the registers it keeps around that call are the called functions' own, not counted
+  here).  The aligned kernels then spill nothing.  The misaligned ones (one more 16-byte
+  unit and a shift per block) reload up to 28 bytes; the test caps them there.
 """
 import os
 import re
