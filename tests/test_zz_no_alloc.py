@@ -55,6 +55,40 @@ def test_noalloc_matches_the_oracle_call_after_call():
     assert binding.blake3_device_status() == 0
 
 
+def _oracle_digest_16_parts(host, key):
+    """The oracle's digest of a power-of-two number of chunks, from 16 aligned subtrees
+    hashed on 16 host threads (the unchanged oracle functions) and folded: the tree of
+    2^k chunks is the perfect tree over those subtrees."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    n = host.numel()
+    part = n // 16
+    assert part % 1024 == 0 and (part // 1024) & (part // 1024 - 1) == 0
+    with ThreadPoolExecutor(16) as ex:
+        cvs = list(ex.map(lambda i: oracle.subtree_cv(host[i * part:(i + 1) * part], key, i * (part // 1024)),
+                          range(16)))
+    while len(cvs) > 2:
+        cvs = [oracle.parent_cv(key, cvs[i], cvs[i + 1]) for i in range(0, len(cvs), 2)]
+    return oracle.parent_cv(key, cvs[0], cvs[1], True)
+
+
+def test_noalloc_at_the_maximum_length():
+    """B3G_NOALLOC_MAX_LEN itself: 16 GiB, 131,072 CTA subtrees of 128 chunks, the most
+    roots the scratch holds, with the tile counter at its end; twice in a row, against
+    the oracle (16 aligned subtrees on host threads, folded)."""
+    build.build()
+    lib = binding.library()
+    key = workloads.key_bytes(11)
+    dev = workloads.uniform_bytes(16, MAX_LEN, device="cuda")
+    got = [_noalloc(lib, dev, key) for _ in range(2)]
+    host = dev.cpu()
+    del dev
+    torch.cuda.empty_cache()
+    want = _oracle_digest_16_parts(host, key)
+    assert got[0] == want and got[1] == want
+    assert binding.blake3_device_status() == 0
+
+
 def test_noalloc_rejects_inputs_over_the_limit():
     build.build()
     lib = binding.library()
