@@ -501,6 +501,15 @@ using namespace b3g;
 // needs no SM-wide parallelism (small pieces, range reductions, the sequential stack
 // records) runs on the high-priority side stream `aux`, ordered against the caller's
 // stream with events, so that it overlaps the leaf launches on the caller's stream.
+//
+// A hasher of its own (blake3_hasher_new) has a second side stream, `rd`, for the work
+// that reads the caller's segment or acc: the small pieces and the copy of a single
+// pushed chunk into one of kChunkSlots staging slots.  The caller's stream then waits
+// only for those reads before it reuses the segment or rewrites acc, not for the chain
+// of records and reductions queued on `aux`, which waits for every leaf launch and runs
+// slowly while the next leaf launch fills the SMs.
+constexpr int kChunkSlots = 4;
+
 struct b3g_hasher {
     uint8_t key[32];      // the key, or the IV (little-endian) in the default mode
     uint32_t kw[8];
@@ -518,6 +527,12 @@ struct b3g_hasher {
     uint32_t depth;     // stack entries
     cudaStream_t aux;   // side stream
     cudaEvent_t ev_fork, ev_read, ev_done;
+    cudaStream_t rd;    // second side stream (NULL: everything on aux)
+    cudaEvent_t ev_fork_rd, ev_read_rd, ev_rd_done, ev_rd_all;
+    bool rd_pending;    // rd has reads that the caller's stream has not waited for
+    uint8_t *slots;     // device: kChunkSlots staging slots of 1024 bytes (with rd)
+    cudaEvent_t ev_slot[kChunkSlots];  // recorded on aux after the chain read slot k
+    uint32_t slot_next;
 };
 
 namespace {
@@ -539,29 +554,54 @@ b3g_status mark_read(b3g_hasher *h) {
     return B3G_OK;
 }
 
-// `s` waits for those reads: afterwards the segment may be reused and acc rewritten
-b3g_status join_reads(b3g_hasher *h, cudaStream_t s) {
-    if (!h->read_pending) return B3G_OK;
-    cudaError_t e = cudaStreamWaitEvent(s, h->ev_read, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
-    h->read_pending = false;
+// rd waits until `s` reaches this point
+b3g_status fork_rd(b3g_hasher *h, cudaStream_t s) {
+    cudaError_t e = cudaEventRecord(h->ev_fork_rd, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->rd, h->ev_fork_rd, 0);
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "fork to the readers' stream");
+}
+
+// rd's reads of segments and of acc, so far, end here; and aux waits for rd's work so
+// far (the piece roots, a staged chunk) before its next launch
+b3g_status rd_handoff(b3g_hasher *h) {
+    cudaError_t e = cudaEventRecord(h->ev_read_rd, h->rd);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_rd_done, h->rd);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->aux, h->ev_rd_done, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "hand over from the readers' stream");
+    h->rd_pending = true;
     return B3G_OK;
 }
 
-// `s` waits for everything queued on the side stream
+// `s` waits for those reads: afterwards the segment may be reused and acc rewritten
+b3g_status join_reads(b3g_hasher *h, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    if (h->read_pending) e = cudaStreamWaitEvent(s, h->ev_read, 0);
+    if (e == cudaSuccess && h->rd_pending) e = cudaStreamWaitEvent(s, h->ev_read_rd, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+    h->read_pending = h->rd_pending = false;
+    return B3G_OK;
+}
+
+// `s` waits for everything queued on the side streams
 b3g_status join_all(b3g_hasher *h, cudaStream_t s) {
     cudaError_t e = cudaEventRecord(h->ev_done, h->aux);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_done, 0);
+    if (e == cudaSuccess && h->rd) e = cudaEventRecord(h->ev_rd_all, h->rd);
+    if (e == cudaSuccess && h->rd) e = cudaStreamWaitEvent(s, h->ev_rd_all, 0);
     if (e != cudaSuccess) return cuda_fail(e, "join the side stream");
-    h->read_pending = false;
+    h->read_pending = h->rd_pending = false;
     return B3G_OK;
 }
 
 b3g_status streams_init(b3g_hasher *h, bool own) {
     h->own_streams = own;
-    h->read_pending = false;
-    h->aux = nullptr;
+    h->read_pending = h->rd_pending = false;
+    h->aux = h->rd = nullptr;
     h->ev_fork = h->ev_read = h->ev_done = nullptr;
+    h->ev_fork_rd = h->ev_read_rd = h->ev_rd_done = h->ev_rd_all = nullptr;
+    h->slots = nullptr;
+    for (cudaEvent_t &ev : h->ev_slot) ev = nullptr;
+    h->slot_next = 0;
     cudaError_t e = cudaSuccess;
     if (own) {
         int least = 0, greatest = 0;
@@ -575,17 +615,41 @@ b3g_status streams_init(b3g_hasher *h, bool own) {
     cudaEvent_t *evs[3] = {&h->ev_fork, &h->ev_read, &h->ev_done};
     for (cudaEvent_t *ev : evs)
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "cudaEventCreateWithFlags");
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreateWithFlags");
+    if (!own) return B3G_OK;
+    // the readers' stream, its events and the chunk staging slots
+    int least = 0, greatest = 0;
+    e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->rd, cudaStreamNonBlocking, greatest);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithPriority");
+    cudaEvent_t *rd_evs[4] = {&h->ev_fork_rd, &h->ev_read_rd, &h->ev_rd_done, &h->ev_rd_all};
+    for (cudaEvent_t *ev : rd_evs)
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    for (cudaEvent_t &ev : h->ev_slot)
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreateWithFlags");
+    e = alloc_sync(reinterpret_cast<void **>(&h->slots), kChunkSlots * kChunkBytes);
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "chunk staging slots");
 }
 
 void streams_release(b3g_hasher *h) {
     if (h->aux) cudaStreamSynchronize(h->aux);
-    cudaEvent_t evs[3] = {h->ev_fork, h->ev_read, h->ev_done};
+    if (h->rd) cudaStreamSynchronize(h->rd);
+    cudaEvent_t evs[7] = {h->ev_fork, h->ev_read, h->ev_done, h->ev_fork_rd, h->ev_read_rd, h->ev_rd_done,
+                          h->ev_rd_all};
     for (cudaEvent_t ev : evs)
         if (ev) cudaEventDestroy(ev);
+    for (cudaEvent_t &ev : h->ev_slot) {
+        if (ev) cudaEventDestroy(ev);
+        ev = nullptr;
+    }
     if (h->own_streams && h->aux) cudaStreamDestroy(h->aux);
-    h->aux = nullptr;
+    if (h->rd) cudaStreamDestroy(h->rd);  // only a hasher's own streams have rd
+    if (h->slots) cudaFree(h->slots);
+    h->aux = h->rd = nullptr;
+    h->slots = nullptr;
     h->ev_fork = h->ev_read = h->ev_done = nullptr;
+    h->ev_fork_rd = h->ev_read_rd = h->ev_rd_done = h->ev_rd_all = nullptr;
 }
 
 // The aligned power-of-two pieces of the chunk run [pos, pos + n): at every position
@@ -657,16 +721,44 @@ b3g_status push_pieces_one_by_one(b3g_hasher *h, const uint8_t *p, const std::ve
 }
 
 // One full chunk at `p`: a record launch on the side stream merges and pushes its CV.
+// With the readers' stream the chunk is first copied there into a staging slot, which
+// the record reads instead of `p`.
 b3g_status push_one(b3g_hasher *h, const uint8_t *p, cudaStream_t s) {
-    b3g_status st = fork_aux(h, s);
+    const uint8_t *src = p;
+    uint32_t k = 0;
+    b3g_status st = B3G_OK;
+    // under stream capture the slot events (recorded outside the capture) cannot be
+    // waited for: the chunk is read in place, as without the readers' stream
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const cudaError_t ce = cudaStreamIsCapturing(s, &cap);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamIsCapturing");
+    const bool staged = h->rd && cap == cudaStreamCaptureStatusNone;
+    if (staged) {
+        k = h->slot_next++ % kChunkSlots;
+        uint8_t *slot = h->slots + kChunkBytes * k;
+        st = fork_rd(h, s);
+        // the chain has read what this slot held before
+        cudaError_t e = st == B3G_OK ? cudaStreamWaitEvent(h->rd, h->ev_slot[k], 0) : cudaSuccess;
+        if (e == cudaSuccess && st == B3G_OK) e = cudaMemcpyAsync(slot, p, kChunkBytes, cudaMemcpyDeviceToDevice, h->rd);
+        if (e != cudaSuccess) return cuda_fail(e, "chunk staging copy");
+        if (st == B3G_OK) st = rd_handoff(h);
+        src = slot;
+    } else {
+        st = fork_aux(h, s);
+    }
     if (st != B3G_OK) return st;
     RecordArgs ra = record_args(h->state, h->kw, h->mode_flags, kRecPush);
-    ra.in = p;
+    ra.in = src;
     ra.depth = h->depth;
     ra.target = popcount64(h->pushed);
     ra.pushed = h->pushed;
     st = launch_record(ra, h->aux);
-    if (st == B3G_OK) st = mark_read(h);
+    if (st == B3G_OK && staged) {
+        const cudaError_t e = cudaEventRecord(h->ev_slot[k], h->aux);
+        if (e != cudaSuccess) st = cuda_fail(e, "cudaEventRecord");
+    } else if (st == B3G_OK) {
+        st = mark_read(h);
+    }
     if (st == B3G_OK) {
         h->depth = ra.target + 1;
         h->pushed += 1;
@@ -721,7 +813,10 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
     uint8_t *tile_cvs = scratch + roots_bytes;
     uint8_t *huge = tile_cvs + tiles_bytes;
     const cudaStream_t x = h->aux;
-    b3g_status st = fork_aux(h, s);  // the side stream sees the segment and the scratch
+    // the side stream sees the segment and the scratch; so does the readers' stream,
+    // which runs the small pieces when the hasher has one
+    const cudaStream_t xp = h->rd && !small.empty() ? h->rd : x;
+    b3g_status st = xp == x ? fork_aux(h, s) : fork_rd(h, s);
     if (st != B3G_OK) {
         cudaFreeAsync(scratch, s);
         return st;
@@ -741,9 +836,11 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
             pa.nchunks[i] = static_cast<uint32_t>(pc.size);
             pa.slot[i] = static_cast<uint32_t>(small[i]);
         }
-        pieces_kernel<<<static_cast<unsigned>(small.size()), 64, 0, x>>>(pa);
+        pieces_kernel<<<static_cast<unsigned>(small.size()), 64, 0, xp>>>(pa);
         e = cudaGetLastError();
-        st = e == cudaSuccess ? mark_read(h) : cuda_fail(e, "pieces_kernel launch");
+        // the roots go to the chain on aux (rd_handoff makes it wait for them)
+        if (e != cudaSuccess) st = cuda_fail(e, "pieces_kernel launch");
+        else st = xp == x ? mark_read(h) : rd_handoff(h);
     }
     if (st == B3G_OK && !big.empty()) {
         uint32_t *status = nullptr;
@@ -953,9 +1050,13 @@ b3g_status host_range(const void *h_in, uint64_t len, const uint8_t key[32], uin
     key_words(key, h.kw);
     h.mode_flags = mode_flags;
     hasher_clear(&h);
-    h.own_streams = h.read_pending = false;
-    h.aux = nullptr;
+    h.own_streams = h.read_pending = h.rd_pending = false;
+    h.aux = h.rd = nullptr;
     h.ev_fork = h.ev_read = h.ev_done = nullptr;
+    h.ev_fork_rd = h.ev_read_rd = h.ev_rd_done = h.ev_rd_all = nullptr;
+    for (cudaEvent_t &ev : h.ev_slot) ev = nullptr;
+    h.slots = nullptr;
+    h.slot_next = 0;
     h.state = base;
     h.acc = base + kBufOff;
     h.acc_cap = kChunkBytes;
