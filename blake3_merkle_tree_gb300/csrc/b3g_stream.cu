@@ -720,41 +720,18 @@ b3g_status push_pieces_one_by_one(b3g_hasher *h, const uint8_t *p, const std::ve
     return st != B3G_OK ? st : rs;
 }
 
-// One full chunk at `p`: a record launch on the side stream merges and pushes its CV.
-// With the readers' stream the chunk is first copied there into a staging slot, which
-// the record reads instead of `p`.
-b3g_status push_one(b3g_hasher *h, const uint8_t *p, cudaStream_t s) {
-    const uint8_t *src = p;
-    uint32_t k = 0;
-    b3g_status st = B3G_OK;
-    // under stream capture the slot events (recorded outside the capture) cannot be
-    // waited for: the chunk is read in place, as without the readers' stream
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    const cudaError_t ce = cudaStreamIsCapturing(s, &cap);
-    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamIsCapturing");
-    const bool staged = h->rd && cap == cudaStreamCaptureStatusNone;
-    if (staged) {
-        k = h->slot_next++ % kChunkSlots;
-        uint8_t *slot = h->slots + kChunkBytes * k;
-        st = fork_rd(h, s);
-        // the chain has read what this slot held before
-        cudaError_t e = st == B3G_OK ? cudaStreamWaitEvent(h->rd, h->ev_slot[k], 0) : cudaSuccess;
-        if (e == cudaSuccess && st == B3G_OK) e = cudaMemcpyAsync(slot, p, kChunkBytes, cudaMemcpyDeviceToDevice, h->rd);
-        if (e != cudaSuccess) return cuda_fail(e, "chunk staging copy");
-        if (st == B3G_OK) st = rd_handoff(h);
-        src = slot;
-    } else {
-        st = fork_aux(h, s);
-    }
-    if (st != B3G_OK) return st;
+// The record that merges the stack down and pushes the CV of the chunk at `src` (on the
+// side stream); `slot` >= 0: `src` is that staging slot, released when the record has
+// read it.
+b3g_status push_record(b3g_hasher *h, const uint8_t *src, int slot) {
     RecordArgs ra = record_args(h->state, h->kw, h->mode_flags, kRecPush);
     ra.in = src;
     ra.depth = h->depth;
     ra.target = popcount64(h->pushed);
     ra.pushed = h->pushed;
-    st = launch_record(ra, h->aux);
-    if (st == B3G_OK && staged) {
-        const cudaError_t e = cudaEventRecord(h->ev_slot[k], h->aux);
+    b3g_status st = launch_record(ra, h->aux);
+    if (st == B3G_OK && slot >= 0) {
+        const cudaError_t e = cudaEventRecord(h->ev_slot[slot], h->aux);
         if (e != cudaSuccess) st = cuda_fail(e, "cudaEventRecord");
     } else if (st == B3G_OK) {
         st = mark_read(h);
@@ -764,6 +741,40 @@ b3g_status push_one(b3g_hasher *h, const uint8_t *p, cudaStream_t s) {
         h->pushed += 1;
     }
     return st;
+}
+
+// A staging slot for a chunk assembled on the readers' stream from up to two pieces
+// (a, na bytes; then b, nb bytes; na + nb = 1024), after `s` has reached this point and
+// the chain has released the slot.  Returns the slot's index in *slot.
+b3g_status stage_chunk_rd(b3g_hasher *h, const uint8_t *a, uint64_t na, const uint8_t *b, uint64_t nb,
+                          cudaStream_t s, int *slot) {
+    const uint32_t k = h->slot_next++ % kChunkSlots;
+    uint8_t *dst = h->slots + kChunkBytes * k;
+    b3g_status st = fork_rd(h, s);
+    if (st != B3G_OK) return st;
+    cudaError_t e = cudaStreamWaitEvent(h->rd, h->ev_slot[k], 0);
+    if (e == cudaSuccess && na) e = cudaMemcpyAsync(dst, a, na, cudaMemcpyDeviceToDevice, h->rd);
+    if (e == cudaSuccess && nb) e = cudaMemcpyAsync(dst + na, b, nb, cudaMemcpyDeviceToDevice, h->rd);
+    if (e != cudaSuccess) return cuda_fail(e, "chunk staging copy");
+    *slot = static_cast<int>(k);
+    return rd_handoff(h);
+}
+
+// One full chunk at `p`: a record launch on the side stream merges and pushes its CV.
+// With the readers' stream the chunk is first copied there into a staging slot, which
+// the record reads instead of `p`; under stream capture (the slots' events were
+// recorded outside the capture) it is read in place.
+b3g_status push_one(b3g_hasher *h, const uint8_t *p, cudaStream_t s) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const cudaError_t ce = cudaStreamIsCapturing(s, &cap);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamIsCapturing");
+    if (h->rd && cap == cudaStreamCaptureStatusNone) {
+        int slot = -1;
+        const b3g_status st = stage_chunk_rd(h, p, kChunkBytes, nullptr, 0, s, &slot);
+        return st == B3G_OK ? push_record(h, h->slots + kChunkBytes * slot, slot) : st;
+    }
+    const b3g_status st = fork_aux(h, s);
+    return st == B3G_OK ? push_record(h, p, -1) : st;
 }
 
 // Push the chunks [h->pushed, h->pushed + nchunks) that start at `p`.  Batched: the
@@ -907,6 +918,40 @@ b3g_status push_run(b3g_hasher *h, const uint8_t *p, uint64_t nchunks, cudaStrea
     }
     e = cudaFreeAsync(scratch, x);
     if (st == B3G_OK && e != cudaSuccess) st = cuda_fail(e, "cudaFreeAsync");
+    return st;
+}
+
+// A segment longer than acc while acc holds less than one chunk, on a hasher with the
+// readers' stream, outside stream capture: the readers' stream assembles the boundary
+// chunk (acc's bytes, then the segment's first `fill`) in a staging slot and, after the
+// whole chunks have been pushed, copies the segment's last bytes into acc, so the
+// caller's stream runs no copy of its own between two leaf launches.
+b3g_status update_long(b3g_hasher *h, const uint8_t *p, uint64_t len, uint64_t fill, cudaStream_t s) {
+    b3g_status st = B3G_OK;
+    if (fill) {
+        int slot = -1;
+        st = stage_chunk_rd(h, h->acc, h->acc_len, p, fill, s, &slot);
+        if (st == B3G_OK) st = push_record(h, h->slots + kChunkBytes * slot, slot);
+        if (st != B3G_OK) return st;
+        h->acc_len = 0;
+    }
+    const uint64_t full = (len - fill) / kChunkBytes;
+    st = push_run(h, p + fill, full, s);
+    if (st != B3G_OK) return st;
+    const uint64_t tail = len - fill - full * kChunkBytes;
+    if (tail) {
+        st = fork_rd(h, s);
+        const cudaError_t e = st == B3G_OK ? cudaMemcpyAsync(h->acc, p + fill + full * kChunkBytes, tail,
+                                                             cudaMemcpyDeviceToDevice, h->rd)
+                                           : cudaSuccess;
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+        if (st == B3G_OK) st = rd_handoff(h);
+        if (st != B3G_OK) return st;
+        h->acc_len = tail;
+    }
+    // the segment may be reused and acc read on `s` once the readers are done
+    st = join_reads(h, s);
+    if (st == B3G_OK) h->count += len;
     return st;
 }
 
@@ -1216,6 +1261,10 @@ b3g_status blake3_hasher_update(b3g_hasher *h, const void *d_in, uint64_t len, b
         st = append_acc(h, p, len, s);
         if (st == B3G_OK) h->count += len;
         return st;
+    }
+    if (h->rd && !capturing && h->acc_len < kChunkBytes) {
+        const uint64_t fill = h->acc_len ? kChunkBytes - h->acc_len : 0;
+        if (len - fill > h->acc_cap) return update_long(h, p, len, fill, s);
     }
     // more than acc holds, so more input follows every chunk in acc: complete its last
     // chunk, push all of acc, then push the segment's whole chunks if they do not fit
