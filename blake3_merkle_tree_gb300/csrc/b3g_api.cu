@@ -178,16 +178,16 @@ b3g_status hash_range(const void *d_in, uint64_t len, uint64_t chunk_offset, con
         // reduction kernel); its ticket counter sits after the tile CVs
         a.ticket = reinterpret_cast<uint32_t *>(ws + round16(a.n_tiles * 32));
         a.final_out = d_out32;
-        cudaError_t e = cudaMemsetAsync(a.ticket, 0, sizeof(uint32_t), stream);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(ticket)");
+        st = launch_zero_word(a.ticket, stream);
+        if (st != B3G_OK) return st;
         return launch_leaf(a, t, false, stream);
     }
     const int g = reduce_group_log2(a.n_tiles);
     if (a.n_tiles > kDynamicMinTiles && leaf_takes_tile_counter(d_in, a.n_full)) {
         // the tile counter sits after the reduction levels
         a.tile_counter = reinterpret_cast<uint32_t *>(ws + round16(a.n_tiles * 32) + reduce_ws(a.n_tiles, g));
-        cudaError_t e = cudaMemsetAsync(a.tile_counter, 0, sizeof(uint32_t), stream);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(tile counter)");
+        st = launch_zero_word(a.tile_counter, stream);
+        if (st != B3G_OK) return st;
     }
     st = launch_leaf(a, t, false, stream);
     if (st != B3G_OK) return st;

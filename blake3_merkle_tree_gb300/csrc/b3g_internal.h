@@ -108,6 +108,10 @@ const char *kernel_config();
 // One level of CV reduction.
 b3g_status launch_reduce(const ReduceArgs &args, cudaStream_t stream);
 
+// Zeroes one device word in stream order (a one-thread kernel launched with
+// programmatic stream serialization, so that the launch behind it overlaps it).
+b3g_status launch_zero_word(uint32_t *p, cudaStream_t stream);
+
 // One-thread bounded-wait probe; writes 1 to *d_flag if the wait gave up.
 b3g_status launch_wait_probe(uint64_t limit_ns, int *d_flag, cudaStream_t stream);
 // The same probe, ORing B3G_DEVICE_STATUS_TIMEOUT into *d_status (stream ordered) if the wait gave up.

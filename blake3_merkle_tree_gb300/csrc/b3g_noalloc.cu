@@ -125,8 +125,8 @@ extern "C" b3g_status blake3_keyed_hash_noalloc(const void *d_in, uint64_t len, 
     a.out = scratch;
     if (tiles > kDynamicMinTiles && leaf_takes_tile_counter(d_in, a.n_full)) {
         a.tile_counter = reinterpret_cast<uint32_t *>(scratch + kNoAllocCounterOffset);
-        const cudaError_t e = cudaMemsetAsync(a.tile_counter, 0, sizeof(uint32_t), s);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(noalloc tile counter)");
+        st = launch_zero_word(a.tile_counter, s);
+        if (st != B3G_OK) return st;
     }
     st = launch_leaf(a, t, false, s);
     if (st != B3G_OK) return st;

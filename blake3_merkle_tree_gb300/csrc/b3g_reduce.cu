@@ -218,6 +218,22 @@ b3g_status launch_compress_rate(uint32_t blocks, uint32_t iters, uint32_t *d_sin
     return e == cudaSuccess ? B3G_OK : cuda_fail(e, "compress_rate_kernel launch");
 }
 
+// Sets one device word to zero in stream order.  A kernel launched with programmatic
+// stream serialization, unlike a memset, lets the launch behind it (the leaf kernel,
+// which waits for this grid in griddepcontrol.wait before it touches the word) start
+// early; and it waits itself for the kernel ahead, which may still use the word (an
+// earlier call on the same workspace).
+__global__ void __launch_bounds__(32) zero_word_kernel(uint32_t *p) {
+    grid_dependency_wait();
+    if (threadIdx.x == 0) *p = 0u;
+    launch_dependents();
+}
+
+b3g_status launch_zero_word(uint32_t *p, cudaStream_t stream) {
+    const cudaError_t e = launch_pdl(zero_word_kernel, dim3(1), dim3(32), 0, stream, p);
+    return e == cudaSuccess ? B3G_OK : cuda_fail(e, "zero_word_kernel launch");
+}
+
 b3g_status launch_reduce(const ReduceArgs &a, cudaStream_t stream) {
     if (a.count == 0 || a.group < 2 || a.group > 2 * kReduceMaxThreads || (a.group & (a.group - 1)) != 0)
         return B3G_ERR_ARG;
