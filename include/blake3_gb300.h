@@ -80,11 +80,11 @@ int blake3_default_leaves_log2(void);
  * after the change). */
 typedef enum {
     /* 0 (default) or 1.  With 1, an input of at most 32 CTA subtrees is reduced to its
-     * digest by the CTA that finishes last (an atomic ticket counter, zeroed by a 4-byte
-     * memset on the stream) instead of by a second kernel launch.  Measured on GB300 it
-     * is slower for 1 MiB (24.6 vs 22.5 us per digest in a CUDA graph): the memset costs
-     * more than the launch it saves.  Applies to 16-byte aligned inputs with at least
-     * one full chunk. */
+     * digest by the CTA that finishes last (an atomic ticket counter, zeroed on the
+     * stream by a one-thread kernel) instead of by a second kernel launch.  Measured on
+     * GB300 it is slower for 1 MiB (22.9 vs 21.0 us per digest in a CUDA graph): the
+     * zeroing costs more than the launch it saves.  Applies to 16-byte aligned inputs
+     * with at least one full chunk. */
     B3G_OPT_FUSED_FINAL = 1,
     /* Test hook for failure handling (no GPU fault involved): with value n > 0, the n-th
      * next device allocation the library makes fails as if the device were out of memory
@@ -441,8 +441,8 @@ b3g_status blake3_hash_host(const void *h_in, uint64_t len, uint8_t out32[32], v
  *     Calls whose work overlaps on the GPU (concurrent streams, or several host
  *     threads on one device) race on it and give wrong digests; serialise them.
  *     Within one call everything read from the scratch is written first (the tile
- *     counter is cleared with a memset on `stream`), so leftovers of an earlier call
- *     do no harm.
+ *     counter is cleared by a one-thread kernel on `stream`), so leftovers of an
+ *     earlier call do no harm.
  * Errors: B3G_ERR_NULL, B3G_ERR_ALIGN (d_out32), B3G_ERR_WORKSPACE (len too large),
  * B3G_ERR_CUDA.
  */
