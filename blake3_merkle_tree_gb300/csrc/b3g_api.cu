@@ -132,16 +132,22 @@ LeafArgs leaf_args(const void *d_in, uint64_t len, uint64_t chunk_offset, const 
 }
 
 // Chunks per CTA subtree (log2) for an input of n chunks.  Large inputs use
-// 2^kDefaultLeavesLog2 (128).  For an input of at most 2^16 chunks (64 MiB) the
-// subtree shrinks (down to 32 chunks) until there are at least kSpreadTiles CTAs: each chunk is a chain of 16 dependent compressions, so small inputs finish
-// sooner with fewer warps per SM.  A function of n alone, so that the workspace size
-// is a function of the length alone.
+// 2^kDefaultLeavesLog2 (128).  For an input of at most 2^16 chunks (64 MiB) with fewer
+// than kFullTileMinTiles subtrees of that size, the subtree shrinks (down to 32 chunks)
+// until there are at least kSpreadTiles CTAs: each chunk is a chain of 16 dependent
+// compressions, so small inputs finish sooner with fewer warps per SM.  From
+// kFullTileMinTiles 128-chunk subtrees on (10 MiB), the 128-chunk kernel with at most
+// one CTA per SM is faster than the smaller subtrees' kernels (measured on GB300: 10 MiB
+// 364 against 330 GB/s, 12 MiB 436 against 391, 16 MiB 579 against 515; at 8 MiB, 64
+// subtrees, it is not).  A function of n alone, so that the workspace size is a function
+// of the length alone.
 constexpr uint64_t kSmallInputChunks = 1ull << 16;
 constexpr uint64_t kSpreadTiles = 152;
+constexpr uint64_t kFullTileMinTiles = 80;
 
 int choose_leaves_log2(uint64_t n_chunks) {
     int t = kDefaultLeavesLog2;
-    if (n_chunks <= kSmallInputChunks)
+    if (n_chunks <= kSmallInputChunks && ceil_div(n_chunks, 1ull << t) < kFullTileMinTiles)
         while (t > kMinLeavesLog2 && ceil_div(n_chunks, 1ull << t) < kSpreadTiles) --t;
     return t;
 }

@@ -65,8 +65,12 @@ def test_sizes(lib):
     # 128-chunk tiles already give 512 CTAs, reduced 512 -> 8 -> 1
     assert lib.blake3_workspace_size(64 << 20) == 512 * 32 + 8 * 32
     assert lib.blake3_workspace_size(19 << 20) == 152 * 32 + 3 * 32  # 19456 chunks / 128
-    # 144 tiles of 128 < 152: 64-chunk tiles, 288 -> 5 -> 1
-    assert lib.blake3_workspace_size(18 << 20) == 288 * 32 + 5 * 32
+    # 144 tiles of 128: fewer than one per SM, but at least 80 keep 128-chunk tiles,
+    # 144 -> 3 -> 1 (10 MiB: 80 -> 2 -> 1); below 80 (9 MiB: 72) the tiles shrink until
+    # there are 152: 32 chunks, 288 -> 5 -> 1
+    assert lib.blake3_workspace_size(18 << 20) == 144 * 32 + 3 * 32
+    assert lib.blake3_workspace_size(10 << 20) == 80 * 32 + 2 * 32
+    assert lib.blake3_workspace_size(9 << 20) == 288 * 32 + 5 * 32
     # 4 GiB: 32768 tile CVs, then 512 and 8 group CVs, then 16 bytes for the tile counter
     # (more tiles than one per resident CTA)
     assert lib.blake3_workspace_size(1 << 32) == 32768 * 32 + 512 * 32 + 8 * 32 + 16
