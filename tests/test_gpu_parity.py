@@ -256,3 +256,20 @@ def test_one_shot_digest_with_tile_counter(tiles, offset):
     assert bytes(binding.blake3_keyed_hash(dev, KEY).cpu().numpy()) == want
     if tiles == 761 and offset == 0:
         assert bytes(binding.blake3_hash_ws(dev, ws).cpu().numpy()) == oracle.hash(host)
+
+
+@pytest.mark.parametrize("length,offset", [(9 << 20, 0), ((10 << 20) - 1, 0), (10 << 20, 0), ((12 << 20) + 5, 3),
+                                           ((18 << 20) + 777, 0), ((19 << 20) - 1, 8)])
+def test_one_shot_digest_around_the_subtree_size_rule(length, offset):
+    """The one-shot digest chooses its CTA subtree size from the length: 32 to 64 chunks
+    below 80 subtrees of 128, 128 chunks from 80 of them on (10 MiB) even with fewer than
+    one CTA per SM.  Lengths on both sides of that step, aligned and misaligned, against
+    the oracle, with the workspace the size function gives."""
+    host = workloads.uniform_bytes(length + offset, length)
+    buf = torch.empty(length + offset, dtype=torch.uint8, device="cuda")
+    buf[offset:].copy_(host)
+    dev = buf[offset:]
+    want = oracle.keyed_hash(host, KEY)
+    ws = torch.full((max(16, binding.blake3_workspace_size(length)),), 0x5A, dtype=torch.uint8, device="cuda")
+    assert bytes(binding.blake3_keyed_hash_ws(dev, KEY, ws).cpu().numpy()) == want
+    assert bytes(binding.blake3_keyed_hash(dev, KEY).cpu().numpy()) == want
